@@ -1,0 +1,87 @@
+"""Seeded synthetic inputs and the workload table for the tensor-parallel MLP block.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle's tests.
+It holds no arithmetic of the block itself: it only draws normal random numbers,
+scales them by a standard deviation and rounds them to bf16.
+
+Recipe (per workload, one ``torch.Generator('cpu')`` seeded with ``seed``):
+draw, in this order, X [T,h], A [h,f], a [f], B [f,h], b [h], dY [T,h] as
+``torch.randn(..., dtype=float32) * sigma`` and round to bf16 (round to nearest even).
+sigma is a standard deviation. The workloads are the GPT layer shapes of
+"Efficient Large-Scale Language Model Training on GPU Clusters Using Megatron-LM",
+§5 (Table 1 models, s = 2048 synthetic batches, MLP width f = 4h from §3 Fig 5a),
+with micro-batches b chosen so that T = b*s tokens.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int          # tokens (micro-batch x sequence length)
+    h: int          # hidden width
+    f: int          # MLP width (4h)
+    t: int          # tensor-parallel shard count
+    sx: float = 1.0     # std of X
+    sw: float = 0.02    # std of A and B
+    sbias: float = 0.01  # std of a and b
+    sdy: float = 0.01   # std of dY
+    desc: str = ""
+
+    @property
+    def flops_fwd_bwd(self) -> int:
+        """Matmul FLOPs of one forward + backward: 6 GEMMs of 2*T*h*f each."""
+        return 12 * self.T * self.h * self.f
+
+
+WORKLOADS: dict[str, Workload] = {w.name: w for w in [
+    Workload("tiny", 128, 64, 256, 2, sdy=1.0,
+             desc="tiny TP MLP block T=128 h=64 f=256 t=2"),
+    Workload("gpt-1.7b-t1", 16384, 2304, 9216, 1,
+             desc="GPT 1.7B-shaped layer T=16384 (8x2048) h=2304 f=9216 t=1"),
+    Workload("gpt-1.7b-t2", 16384, 2304, 9216, 2,
+             desc="GPT 1.7B-shaped layer T=16384 (8x2048) h=2304 f=9216 t=2"),
+    Workload("gpt-18b", 8192, 6144, 24576, 8,
+             desc="GPT 18B-shaped layer T=8192 (4x2048) h=6144 f=24576 t=8"),
+    Workload("gpt3-175b", 4096, 12288, 49152, 8,
+             desc="GPT-3 175B-shaped layer T=4096 (2x2048) h=12288 f=49152 t=8"),
+    Workload("gpt-1t", 2048, 25600, 102400, 8, sw=0.006,
+             desc="1T-shaped layer T=2048 (1x2048) h=25600 f=102400 t=8"),
+]}
+
+NAMES = ("X", "A", "a", "B", "b", "dY")
+
+
+def shapes(T: int, h: int, f: int) -> dict[str, tuple[int, ...]]:
+    return {"X": (T, h), "A": (h, f), "a": (f,), "B": (f, h), "b": (h,), "dY": (T, h)}
+
+
+def make_inputs(T: int, h: int, f: int, *, seed: int = 0, sx: float = 1.0,
+                sw: float = 0.02, sbias: float = 0.01, sdy: float = 0.01,
+                rows: int | None = None) -> dict[str, torch.Tensor]:
+    """Draw the six bf16 inputs on the CPU in the fixed order X, A, a, B, b, dY.
+
+    ``rows`` (optional) keeps only the first ``rows`` tokens of X and dY; the draws are
+    unchanged, so the kept rows are exactly those of the full workload.
+    """
+    g = torch.Generator("cpu").manual_seed(seed)
+    sig = {"X": sx, "A": sw, "a": sbias, "B": sw, "b": sbias, "dY": sdy}
+    out: dict[str, torch.Tensor] = {}
+    for name, shp in shapes(T, h, f).items():
+        v = torch.randn(shp, generator=g, dtype=torch.float32)
+        v.mul_(sig[name])
+        v = v.to(torch.bfloat16)
+        if rows is not None and name in ("X", "dY"):
+            v = v[:rows].contiguous()
+        out[name] = v
+    return out
+
+
+def make_workload_inputs(w: Workload, *, seed: int = 0, rows: int | None = None
+                         ) -> dict[str, torch.Tensor]:
+    return make_inputs(w.T, w.h, w.f, seed=seed, sx=w.sx, sw=w.sw, sbias=w.sbias,
+                       sdy=w.sdy, rows=rows)

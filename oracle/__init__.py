@@ -1,0 +1,180 @@
+"""fp64 CPU oracle for the tensor-parallel MLP block (ctypes front end of mlp_oracle.c).
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import this package. The CUDA path does not import it, and it does not
+import the CUDA path; the two share only the seeded input generator.
+
+Every function returns float64 numpy arrays. Inputs may be numpy arrays or CPU torch
+tensors; bf16 tensors convert to fp64 exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mlp_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACTS = {"gelu_tanh": 0, "gelu_erf": 1, "relu": 2, "identity": 3}
+
+
+def build(force: bool = False) -> str:
+    """Compile mlp_oracle.c into liboracle.so beside it (gcc, -O3, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-D_DEFAULT_SOURCE", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            i64, i32, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+            lib.oracle_act.restype = ctypes.c_double
+            lib.oracle_act.argtypes = [i32, ctypes.c_double]
+            lib.oracle_act_grad.restype = ctypes.c_double
+            lib.oracle_act_grad.argtypes = [i32, ctypes.c_double]
+            lib.oracle_num_threads.restype = i32
+            lib.oracle_set_num_threads.argtypes = [i32]
+            lib.oracle_mlp_forward.restype = i32
+            lib.oracle_mlp_forward.argtypes = [i64, i64, i64, i32] + [dp] * 8
+            lib.oracle_mlp_backward.restype = i32
+            lib.oracle_mlp_backward.argtypes = [i64, i64, i64, i32] + [dp] * 12
+            lib.oracle_mlp_sharded.restype = i32
+            lib.oracle_mlp_sharded.argtypes = [i64, i64, i64, i64, i32] + [dp] * 14
+            lib.oracle_mlp_sampled_bf16.restype = i32
+            lib.oracle_mlp_sampled_bf16.argtypes = ([i64, i64, i64, i32] + [dp] * 6 +
+                                                    [i64, dp, i64, dp] + [dp] * 6)
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _bits(x) -> np.ndarray:
+    """Raw bf16 bit patterns of a CPU torch bf16 tensor, as a contiguous uint16 array."""
+    import torch
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def act(x, kind: str = "gelu_tanh") -> np.ndarray:
+    lib = _load()
+    xs = _f64(x)
+    return np.array([lib.oracle_act(ACTS[kind], float(v)) for v in xs.ravel()]).reshape(xs.shape)
+
+
+def act_grad(x, kind: str = "gelu_tanh") -> np.ndarray:
+    lib = _load()
+    xs = _f64(x)
+    return np.array([lib.oracle_act_grad(ACTS[kind], float(v)) for v in xs.ravel()]).reshape(xs.shape)
+
+
+def forward(X, A, a, B, b, act: str = "gelu_tanh"):
+    """(H, G, Y) of the unsharded block."""
+    lib = _load()
+    X, A, a, B, b = map(_f64, (X, A, a, B, b))
+    T, h = X.shape
+    f = A.shape[1]
+    assert A.shape == (h, f) and a.shape == (f,) and B.shape == (f, h) and b.shape == (h,)
+    H = np.empty((T, f)); G = np.empty((T, f)); Y = np.empty((T, h))
+    rc = lib.oracle_mlp_forward(T, h, f, ACTS[act], _p(X), _p(A), _p(a), _p(B), _p(b),
+                                _p(H), _p(G), _p(Y))
+    assert rc == 0, rc
+    return H, G, Y
+
+
+def backward(X, A, B, H, G, dY, act: str = "gelu_tanh") -> dict:
+    """dX, dA, da, dB, db (and dH) of the unsharded block, from the forward's H and G."""
+    lib = _load()
+    X, A, B, H, G, dY = map(_f64, (X, A, B, H, G, dY))
+    T, h = X.shape
+    f = A.shape[1]
+    out = {"dX": np.empty((T, h)), "dA": np.empty((h, f)), "da": np.empty(f),
+           "dB": np.empty((f, h)), "db": np.empty(h), "dH": np.empty((T, f))}
+    rc = lib.oracle_mlp_backward(T, h, f, ACTS[act], _p(X), _p(A), _p(B), _p(H), _p(G), _p(dY),
+                                 _p(out["dX"]), _p(out["dA"]), _p(out["da"]), _p(out["dB"]),
+                                 _p(out["db"]), _p(out["dH"]))
+    assert rc == 0, rc
+    return out
+
+
+def fwd_bwd(inp: dict, act: str = "gelu_tanh") -> dict:
+    """Every output of one forward + backward: Y, H, G, dX, dA, da, dB, db, dH."""
+    H, G, Y = forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], act)
+    out = backward(inp["X"], inp["A"], inp["B"], H, G, inp["dY"], act)
+    out.update(H=H, G=G, Y=Y)
+    return out
+
+
+def sharded(inp: dict, t: int, act: str = "gelu_tanh", parts: bool = False) -> dict:
+    """The block computed shard by shard with explicit sums over the t shards."""
+    lib = _load()
+    X, A, a, B, b, dY = (_f64(inp[k]) for k in ("X", "A", "a", "B", "b", "dY"))
+    T, h = X.shape
+    f = A.shape[1]
+    out = {"Y": np.empty((T, h)), "dX": np.empty((T, h)), "dA": np.empty((h, f)),
+           "da": np.empty(f), "dB": np.empty((f, h)), "db": np.empty(h)}
+    Yp = np.empty((t, T, h)) if parts else None
+    dXp = np.empty((t, T, h)) if parts else None
+    rc = lib.oracle_mlp_sharded(T, h, f, t, ACTS[act], _p(X), _p(A), _p(a), _p(B), _p(b), _p(dY),
+                                _p(out["Y"]), _p(out["dX"]), _p(out["dA"]), _p(out["da"]),
+                                _p(out["dB"]), _p(out["db"]),
+                                _p(Yp) if parts else None, _p(dXp) if parts else None)
+    if rc != 0:
+        raise ValueError(f"oracle_mlp_sharded rejected T={T} h={h} f={f} t={t} (rc={rc})")
+    if parts:
+        out["Y_part"] = Yp
+        out["dX_part"] = dXp
+    return out
+
+
+def sampled_bf16(inp: dict, rows, cols, act: str = "gelu_tanh") -> dict:
+    """Sampled entries of the block over bf16 inputs (torch bf16 CPU tensors).
+
+    Returns Y_rows [nR,h], dX_rows [nR,h], dA_cols [h,nC], dB_rows [nC,h], da [nC], db [h].
+    """
+    lib = _load()
+    X, A, a, B, b, dY = (_bits(inp[k]) for k in ("X", "A", "a", "B", "b", "dY"))
+    T, h = X.shape
+    f = A.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    nR, nC = len(rows), len(cols)
+    Yr = np.empty((nR, h)); dXr = np.empty((nR, h)); dAc = np.empty((nC, h))
+    dBc = np.empty((nC, h)); dac = np.empty(nC); db = np.empty(h)
+    rc = lib.oracle_mlp_sampled_bf16(T, h, f, ACTS[act], _p(X), _p(A), _p(a), _p(B), _p(b), _p(dY),
+                                     nR, _p(rows), nC, _p(cols), _p(Yr), _p(dXr), _p(dAc), _p(dBc),
+                                     _p(dac), _p(db))
+    assert rc == 0, rc
+    return {"Y_rows": Yr, "dX_rows": dXr, "dA_cols": dAc.T.copy(), "dB_rows": dBc, "da": dac,
+            "db": db}

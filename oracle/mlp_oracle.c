@@ -1,0 +1,401 @@
+/*
+ * mlp_oracle.c -- plain fp64 CPU oracle for the tensor-parallel Transformer MLP block.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the package smoke check and the CPU-baseline leg of
+ * the benchmark load this library. The CUDA path shares no code with it and never calls it.
+ *
+ * What it computes (row-major, rows are tokens):
+ *   H = X*A + a,  G = act(H),  Y = G*B + b                               (forward)
+ *   dG = dY*B^T,  dH = dG (.) act'(H),  dX = dH*A^T,
+ *   dA = X^T*dH,  dB = G^T*dY,  da = colsum(dH),  db = colsum(dY)          (backward)
+ * with X [T,h], A [h,f], a [f], B [f,h], b [h], dY [T,h].
+ *
+ * Sources:
+ *  - "Efficient Large-Scale Language Model Training on GPU Clusters Using Megatron-LM"
+ *    (paper summary), section 3 "Tensor Model Parallelism: The Megatron Partitioning",
+ *    Figure 5a: Y = GeLU(XA), Z = Dropout(YB); A split by columns, B by rows, one sum.
+ *    Section 3 "Fused element-wise kernels" names the bias+GeLU pair, which places the
+ *    first bias before the activation.
+ *  - "Distributed training" (ml-interview-book), section 2.6 "Tensor parallelism: why
+ *    exactly two all-reduces per block": GELU(XA)B = sum_i GELU(XA_i) B_i, and the column
+ *    layer's input gradient is sum_i dY_i W_i^T.
+ *  - "Parallelism" (xuewyang.github.io), "The MLP, with real numbers" and "The backward
+ *    pass": the per-shard backward through B, the nonlinearity and A, the sum for dX, and
+ *    local weight gradients dA_i = X^T dH_i.
+ *
+ * Readings taken where the pages are silent: the activation is the tanh form of GELU
+ * (erf GELU, ReLU with relu'(0) = 0 and the identity are selectable for tests); the output
+ * bias b is added once, after the shard sum, so db = colsum(dY); shards are contiguous equal
+ * column blocks of A (row blocks of B), as torch.chunk makes them.
+ *
+ * Nothing is rounded: inputs arrive as fp64 (or as bf16 bit patterns that convert exactly)
+ * and every sum is carried in fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ACT_GELU_TANH = 0, ACT_GELU_ERF = 1, ACT_RELU = 2, ACT_IDENTITY = 3 };
+
+/* ---- activations ------------------------------------------------------------------ */
+
+/* GELU, tanh form (Hendrycks & Gimpel): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+static double gelu_tanh(double x)
+{
+    const double c = sqrt(2.0 / M_PI);
+    double u = c * (x + 0.044715 * x * x * x);
+    return 0.5 * x * (1.0 + tanh(u));
+}
+
+/* d/dx of the tanh form: 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) du/dx,
+ * du/dx = sqrt(2/pi) (1 + 3 * 0.044715 x^2). */
+static double gelu_tanh_grad(double x)
+{
+    const double c = sqrt(2.0 / M_PI);
+    double u = c * (x + 0.044715 * x * x * x);
+    double th = tanh(u);
+    double du = c * (1.0 + 3.0 * 0.044715 * x * x);
+    return 0.5 * (1.0 + th) + 0.5 * x * (1.0 - th * th) * du;
+}
+
+/* GELU, exact form: x Phi(x), Phi the standard normal CDF. */
+static double gelu_erf(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/* d/dx x Phi(x) = Phi(x) + x phi(x). */
+static double gelu_erf_grad(double x)
+{
+    double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+    double phi = exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+    return Phi + x * phi;
+}
+
+static double act_fn(int act, double x)
+{
+    switch (act) {
+    case ACT_GELU_TANH: return gelu_tanh(x);
+    case ACT_GELU_ERF: return gelu_erf(x);
+    case ACT_RELU: return x > 0.0 ? x : 0.0;
+    default: return x;
+    }
+}
+
+/* ReLU'(0) = 0: "Parallelism" (xuewyang.github.io), "The backward pass", GPU 2's ReLU
+ * passes [2, 1] to [2, 0] because its input was [1, 0]. */
+static double act_grad(int act, double x)
+{
+    switch (act) {
+    case ACT_GELU_TANH: return gelu_tanh_grad(x);
+    case ACT_GELU_ERF: return gelu_erf_grad(x);
+    case ACT_RELU: return x > 0.0 ? 1.0 : 0.0;
+    default: return 1.0;
+    }
+}
+
+double oracle_act(int act, double x) { return act_fn(act, x); }
+double oracle_act_grad(int act, double x) { return act_grad(act, x); }
+
+/* ---- plain matrix products (row-major, fp64) -------------------------------------- */
+
+/* out[M,N] = P[M,K] * Q[K,N] */
+static void mm_nn(int64_t M, int64_t N, int64_t K, const double *P, const double *Q, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double *o = out + i * N;
+        for (int64_t j = 0; j < N; ++j) o[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = P[i * K + k];
+            const double *q = Q + k * N;
+            for (int64_t j = 0; j < N; ++j) o[j] += p * q[j];
+        }
+    }
+}
+
+/* out[M,N] = P[M,K] * Q[N,K]^T */
+static void mm_nt(int64_t M, int64_t N, int64_t K, const double *P, const double *Q, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        const double *p = P + i * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const double *q = Q + j * K;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += p[k] * q[k];
+            out[i * N + j] = s;
+        }
+    }
+}
+
+/* out[M,N] = P[K,M]^T * Q[K,N] */
+static void mm_tn(int64_t M, int64_t N, int64_t K, const double *P, const double *Q, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double *o = out + i * N;
+        for (int64_t j = 0; j < N; ++j) o[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = P[k * M + i];
+            const double *q = Q + k * N;
+            for (int64_t j = 0; j < N; ++j) o[j] += p * q[j];
+        }
+    }
+}
+
+/* out[N] = sum over rows of P[M,N] */
+static void colsum(int64_t M, int64_t N, const double *P, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j) {
+        double s = 0.0;
+        for (int64_t i = 0; i < M; ++i) s += P[i * N + j];
+        out[j] = s;
+    }
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ---- the unsharded block ----------------------------------------------------------- */
+
+/* Forward, Figure 5a with biases: H = X A + a; G = act(H); Y = G B + b.
+ * H, G are [T,f] and are what the forward keeps for the backward ("Distributed training",
+ * section 2.2: the MLP stores the GELU input and the down-projection input). */
+int oracle_mlp_forward(int64_t T, int64_t h, int64_t f, int act,
+                       const double *X, const double *A, const double *a,
+                       const double *B, const double *b,
+                       double *H, double *G, double *Y)
+{
+    if (T < 0 || h < 1 || f < 1) return 1;
+    mm_nn(T, f, h, X, A, H);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t j = 0; j < f; ++j) {
+            double v = H[r * f + j] + a[j];
+            H[r * f + j] = v;
+            G[r * f + j] = act_fn(act, v);
+        }
+    mm_nn(T, h, f, G, B, Y);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t n = 0; n < h; ++n) Y[r * h + n] += b[n];
+    return 0;
+}
+
+/* Backward by the chain rule through Y = G B + b, G = act(H), H = X A + a:
+ * dG = dY B^T; dH = dG (.) act'(H); dX = dH A^T; dA = X^T dH; dB = G^T dY;
+ * da = colsum(dH); db = colsum(dY). dH (optional, [T,f]) is returned when non-NULL. */
+int oracle_mlp_backward(int64_t T, int64_t h, int64_t f, int act,
+                        const double *X, const double *A, const double *B,
+                        const double *H, const double *G, const double *dY,
+                        double *dX, double *dA, double *da, double *dB, double *db,
+                        double *dH_out)
+{
+    if (T < 0 || h < 1 || f < 1) return 1;
+    double *dH = dH_out ? dH_out : (double *)malloc(sizeof(double) * (size_t)(T * f > 0 ? T * f : 1));
+    if (!dH) return 2;
+    mm_nt(T, f, h, dY, B, dH); /* dG */
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t j = 0; j < f; ++j) dH[r * f + j] *= act_grad(act, H[r * f + j]);
+    mm_nt(T, h, f, dH, A, dX);
+    mm_tn(h, f, T, X, dH, dA);
+    mm_tn(f, h, T, G, dY, dB);
+    colsum(T, f, dH, da);
+    colsum(T, h, dY, db);
+    if (!dH_out) free(dH);
+    return 0;
+}
+
+/* ---- the sharded block, shard by shard (the pages' own form) ------------------------ */
+
+/* Shard i owns columns [i f/t, (i+1) f/t) of A and a, and the same rows of B.
+ * Forward: P_i = act(X A_i + a_i) B_i; Y = sum_i P_i + b (the g sum).
+ * Backward: dG_i = dY B_i^T; dH_i = dG_i (.) act'(H_i); dX_i = dH_i A_i^T; dX = sum_i dX_i
+ * (the f sum: the backward of a copy is a sum); dA_i = X^T dH_i; dB_i = G_i^T dY;
+ * da_i = colsum(dH_i); db = colsum(dY).
+ * Y_part and dX_part, when non-NULL, receive the t per-shard partials [t,T,h]. */
+int oracle_mlp_sharded(int64_t T, int64_t h, int64_t f, int64_t t, int act,
+                       const double *X, const double *A, const double *a,
+                       const double *B, const double *b, const double *dY,
+                       double *Y, double *dX, double *dA, double *da, double *dB, double *db,
+                       double *Y_part, double *dX_part)
+{
+    if (T < 0 || h < 1 || f < 1 || t < 1 || f % t != 0) return 1;
+    int64_t fs = f / t;
+    size_t nTf = (size_t)(T * fs > 0 ? T * fs : 1), nhf = (size_t)(h * fs), nTh = (size_t)(T * h > 0 ? T * h : 1);
+    double *Ai = malloc(sizeof(double) * nhf), *Bi = malloc(sizeof(double) * nhf);
+    double *Hi = malloc(sizeof(double) * nTf), *Gi = malloc(sizeof(double) * nTf);
+    double *dHi = malloc(sizeof(double) * nTf), *Pi = malloc(sizeof(double) * nTh);
+    double *dXi = malloc(sizeof(double) * nTh), *dAi = malloc(sizeof(double) * nhf);
+    double *dBi = malloc(sizeof(double) * nhf);
+    if (!Ai || !Bi || !Hi || !Gi || !dHi || !Pi || !dXi || !dAi || !dBi) return 2;
+    for (int64_t i = 0; i < T * h; ++i) { Y[i] = 0.0; dX[i] = 0.0; }
+    for (int64_t s = 0; s < t; ++s) {
+        int64_t c0 = s * fs;
+        for (int64_t k = 0; k < h; ++k)
+            for (int64_t j = 0; j < fs; ++j) Ai[k * fs + j] = A[k * f + c0 + j];
+        for (int64_t j = 0; j < fs; ++j)
+            for (int64_t n = 0; n < h; ++n) Bi[j * h + n] = B[(c0 + j) * h + n];
+        /* column-parallel half: shard-local activation */
+        mm_nn(T, fs, h, X, Ai, Hi);
+        for (int64_t r = 0; r < T; ++r)
+            for (int64_t j = 0; j < fs; ++j) {
+                Hi[r * fs + j] += a[c0 + j];
+                Gi[r * fs + j] = act_fn(act, Hi[r * fs + j]);
+            }
+        /* row-parallel half: partial output, summed over shards */
+        mm_nn(T, h, fs, Gi, Bi, Pi);
+        for (int64_t i = 0; i < T * h; ++i) Y[i] += Pi[i];
+        if (Y_part) memcpy(Y_part + s * T * h, Pi, sizeof(double) * (size_t)(T * h));
+        /* backward through the shard */
+        mm_nt(T, fs, h, dY, Bi, dHi);
+        for (int64_t r = 0; r < T; ++r)
+            for (int64_t j = 0; j < fs; ++j) dHi[r * fs + j] *= act_grad(act, Hi[r * fs + j]);
+        mm_nt(T, h, fs, dHi, Ai, dXi);
+        for (int64_t i = 0; i < T * h; ++i) dX[i] += dXi[i];
+        if (dX_part) memcpy(dX_part + s * T * h, dXi, sizeof(double) * (size_t)(T * h));
+        mm_tn(h, fs, T, X, dHi, dAi);
+        mm_tn(fs, h, T, Gi, dY, dBi);
+        for (int64_t k = 0; k < h; ++k)
+            for (int64_t j = 0; j < fs; ++j) dA[k * f + c0 + j] = dAi[k * fs + j];
+        for (int64_t j = 0; j < fs; ++j)
+            for (int64_t n = 0; n < h; ++n) dB[(c0 + j) * h + n] = dBi[j * h + n];
+        colsum(T, fs, dHi, da + c0);
+    }
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t n = 0; n < h; ++n) Y[r * h + n] += b[n];
+    colsum(T, h, dY, db);
+    free(Ai); free(Bi); free(Hi); free(Gi); free(dHi); free(Pi); free(dXi); free(dAi); free(dBi);
+    return 0;
+}
+
+/* ---- sampled entries over bf16 inputs (large workloads) ---------------------------- */
+
+/* bf16 bit pattern -> fp64, exact: a bf16 is the top half of an IEEE binary32. */
+static double bf16d(uint16_t v)
+{
+    uint32_t u = (uint32_t)v << 16;
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
+
+/* The same block as oracle_mlp_forward/backward, evaluated only where asked, with the
+ * inputs given as bf16 bit patterns:
+ *   for each sampled token r = rows[i]:  Y[r,:] and dX[r,:]   -> Yr[i*h+n], dXr[i*h+k]
+ *   for each sampled column j = cols[c]: dA[:,j], dB[j,:], da[j] -> dAc[c*h+k], dBc[c*h+n], dac[c]
+ *   and all of db.
+ * Each sampled entry is the full sum of its definition; nothing is approximated. */
+int oracle_mlp_sampled_bf16(int64_t T, int64_t h, int64_t f, int act,
+                            const uint16_t *X, const uint16_t *A, const uint16_t *a,
+                            const uint16_t *B, const uint16_t *b, const uint16_t *dY,
+                            int64_t nR, const int64_t *rows, int64_t nC, const int64_t *cols,
+                            double *Yr, double *dXr, double *dAc, double *dBc, double *dac,
+                            double *db)
+{
+    if (T < 1 || h < 1 || f < 1) return 1;
+    for (int64_t i = 0; i < nR; ++i) if (rows[i] < 0 || rows[i] >= T) return 1;
+    for (int64_t c = 0; c < nC; ++c) if (cols[c] < 0 || cols[c] >= f) return 1;
+
+    /* sampled tokens: one row of H, G, dG, dH each */
+#pragma omp parallel
+    {
+        double *x = malloc(sizeof(double) * (size_t)h), *dy = malloc(sizeof(double) * (size_t)h);
+        double *Hr = malloc(sizeof(double) * (size_t)f), *Gr = malloc(sizeof(double) * (size_t)f);
+        double *dHr = malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nR; ++i) {
+            int64_t r = rows[i];
+            for (int64_t k = 0; k < h; ++k) { x[k] = bf16d(X[r * h + k]); dy[k] = bf16d(dY[r * h + k]); }
+            for (int64_t j = 0; j < f; ++j) Hr[j] = 0.0;
+            for (int64_t k = 0; k < h; ++k) {
+                double xk = x[k];
+                const uint16_t *Ak = A + k * f;
+                for (int64_t j = 0; j < f; ++j) Hr[j] += xk * bf16d(Ak[j]);
+            }
+            for (int64_t j = 0; j < f; ++j) {
+                Hr[j] += bf16d(a[j]);
+                Gr[j] = act_fn(act, Hr[j]);
+            }
+            for (int64_t n = 0; n < h; ++n) Yr[i * h + n] = bf16d(b[n]);
+            for (int64_t j = 0; j < f; ++j) {
+                double g = Gr[j], dg = 0.0;
+                const uint16_t *Bj = B + j * h;
+                for (int64_t n = 0; n < h; ++n) {
+                    double bjn = bf16d(Bj[n]);
+                    Yr[i * h + n] += g * bjn;
+                    dg += dy[n] * bjn;
+                }
+                dHr[j] = dg * act_grad(act, Hr[j]);
+            }
+            for (int64_t k = 0; k < h; ++k) {
+                const uint16_t *Ak = A + k * f;
+                double s = 0.0;
+                for (int64_t j = 0; j < f; ++j) s += dHr[j] * bf16d(Ak[j]);
+                dXr[i * h + k] = s;
+            }
+        }
+        free(x); free(dy); free(Hr); free(Gr); free(dHr);
+    }
+
+    /* sampled columns: one column of H, G, dG, dH each, over all tokens */
+#pragma omp parallel
+    {
+        double *Acol = malloc(sizeof(double) * (size_t)h), *Brow = malloc(sizeof(double) * (size_t)h);
+        double *Hc = malloc(sizeof(double) * (size_t)T), *Gc = malloc(sizeof(double) * (size_t)T);
+        double *dHc = malloc(sizeof(double) * (size_t)T);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t c = 0; c < nC; ++c) {
+            int64_t j = cols[c];
+            for (int64_t k = 0; k < h; ++k) Acol[k] = bf16d(A[k * f + j]);
+            for (int64_t n = 0; n < h; ++n) Brow[n] = bf16d(B[j * h + n]);
+            double aj = bf16d(a[j]);
+            for (int64_t r = 0; r < T; ++r) {
+                double s = 0.0, dg = 0.0;
+                for (int64_t k = 0; k < h; ++k) s += bf16d(X[r * h + k]) * Acol[k];
+                Hc[r] = s + aj;
+                Gc[r] = act_fn(act, Hc[r]);
+                for (int64_t n = 0; n < h; ++n) dg += bf16d(dY[r * h + n]) * Brow[n];
+                dHc[r] = dg * act_grad(act, Hc[r]);
+            }
+            double sa = 0.0;
+            for (int64_t r = 0; r < T; ++r) sa += dHc[r];
+            dac[c] = sa;
+            for (int64_t k = 0; k < h; ++k) dAc[c * h + k] = 0.0;
+            for (int64_t n = 0; n < h; ++n) dBc[c * h + n] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                double dh = dHc[r], g = Gc[r];
+                for (int64_t k = 0; k < h; ++k) dAc[c * h + k] += bf16d(X[r * h + k]) * dh;
+                for (int64_t n = 0; n < h; ++n) dBc[c * h + n] += g * bf16d(dY[r * h + n]);
+            }
+        }
+        free(Acol); free(Brow); free(Hc); free(Gc); free(dHc);
+    }
+
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < h; ++n) {
+        double s = 0.0;
+        for (int64_t r = 0; r < T; ++r) s += bf16d(dY[r * h + n]);
+        db[n] = s;
+    }
+    return 0;
+}
