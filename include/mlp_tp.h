@@ -1,0 +1,113 @@
+/*
+ * mlp_tp.h -- C ABI of the tensor-parallel Transformer MLP block on one sm_103a GPU.
+ *
+ * The block (Megatron partitioning, "Efficient Large-Scale Language Model Training on GPU
+ * Clusters Using Megatron-LM", section 3 "Tensor Model Parallelism: The Megatron
+ * Partitioning", Figure 5a; with the biases of the fused bias+GeLU kernel of the same
+ * section):
+ *
+ *     H = X*A + a,    G = GELU(H),    Y = G*B + b
+ *
+ * with A = [A_1 | ... | A_t] split by columns and B = [B_1; ...; B_t] split by rows into
+ * t equal contiguous shards ("Distributed training", ml-interview-book, section 2.6 and
+ * section 3.2, torch.chunk blocks). Every shard's GELU is shard-local and
+ * Y = sum_i GELU(X A_i + a_i) B_i + b; here all t shards live on one GPU and the sum over
+ * shards is the K loop of one tensor-core accumulator (the all-reduce g of the pages
+ * becomes an on-chip sum). Backward, likewise, dX = sum_i dH_i A_i^T (the all-reduce f:
+ * "the backward of a copy is a sum", "Parallelism", xuewyang.github.io, "The backward
+ * pass").
+ *
+ * GELU is the tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *
+ * Layout: every matrix is row-major and dense (row stride = number of columns).
+ *   X [T,h]  A [h,f]  a [f]  B [f,h]  b [h]  H, G [T,f]  Y [T,h]
+ *   dY [T,h] dX [T,h] dA [h,f] dB [f,h] da [f] db [h]
+ * mlp_bf16 is the raw bit pattern of a bfloat16; da and db are fp32.
+ *
+ * Ownership: the caller allocates every buffer (device memory) and owns the stream; the
+ * library allocates no device memory and keeps no pointer after a call returns.
+ *
+ * Execution: calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = the legacy
+ * default stream) of the current device. All arguments are checked before anything is
+ * launched; a failing check returns its status and launches nothing. Launch failures
+ * return MLP_ECUDA. Device-side waits are bounded; a wait that runs out records an error
+ * that mlp_tp_query_device_status() reports as MLP_ETIMEOUT.
+ *
+ * Shapes: T >= 0; h, f >= 8 and multiples of 8; t >= 1 with f % t == 0 and (f/t) % 8 == 0.
+ * Pointers: 16-byte aligned and non-NULL, except that buffers indexed by tokens (X, H, G,
+ * Y, dY, dX) may be NULL when T == 0. Results agree, within bf16 rounding, for every
+ * admissible t (the shard-sum identity), and are bitwise reproducible run to run.
+ */
+#ifndef MLP_TP_H
+#define MLP_TP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLP_OK = 0,
+    MLP_EINVAL = 1,       /* NULL pointer, t < 1, T < 0, h or f < 8 */
+    MLP_ESHAPE = 2,       /* f % t != 0, or h, f, f/t not multiples of 8 */
+    MLP_EALIGN = 3,       /* a pointer is not 16-byte aligned */
+    MLP_ECUDA = 4,        /* a CUDA runtime call or launch failed */
+    MLP_ETIMEOUT = 5,     /* a bounded device-side wait ran out (reported by query) */
+    MLP_EUNSUPPORTED = 6, /* no sm_100-family tensor cores on the current device */
+    MLP_EWORKSPACE = 7    /* workspace smaller than mlp_tp_workspace_bytes() */
+} mlp_status;
+
+typedef uint16_t mlp_bf16;
+
+/* Forward pass: H = X*A + a and G = GELU(H) (first GEMM, bias and GELU in its epilogue),
+ * then Y = G*B + b (second GEMM; its K loop runs over the t shards' row blocks of B into
+ * one accumulator, so the shard sum never leaves the chip). H and G are the activations
+ * the backward needs ("Distributed training", section 2.2: the MLP keeps the GELU input
+ * and the down-projection input). Two kernel launches. */
+mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
+                          const mlp_bf16* B, const mlp_bf16* b, int T, int h, int f, int t,
+                          mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* cuda_stream);
+
+/* Backward pass given dY = dL/dY ("Parallelism", "The backward pass"; chain rule):
+ *   dH = (dY*B^T) (.) GELU'(H)        per shard, GELU' in the GEMM epilogue
+ *   dX = dH*A^T = sum_i dH_i A_i^T    shard sum in one accumulator
+ *   dA = X^T*dH,  dB = G^T*dY         local weight gradients
+ *   da = colsum(dH) (fp32),  db = colsum(dY) (fp32)
+ * `workspace` (device, >= mlp_tp_workspace_bytes(T,h,f,t) bytes, 256-byte aligned) holds
+ * dH and the reduction partials; its contents on entry do not matter. Six launches. */
+mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
+                           const mlp_bf16* H, const mlp_bf16* G, const mlp_bf16* dY,
+                           int T, int h, int f, int t,
+                           mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Device bytes mlp_tp_backward needs as workspace for these sizes (0 on invalid sizes). */
+size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
+
+/* Synchronises `cuda_stream`, then reports and clears the device status word of the
+ * current device: MLP_ETIMEOUT if a bounded device wait ran out since the last query,
+ * MLP_ECUDA if the stream holds a CUDA error, else MLP_OK. */
+mlp_status mlp_tp_query_device_status(void* cuda_stream);
+
+/* The raw device status code behind the last MLP_ETIMEOUT (which wait gave up), or 0. */
+int mlp_tp_last_device_code(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char* mlp_tp_status_string(mlp_status s);
+
+/* Number of kernel launches one forward / one backward call makes for these sizes. */
+int mlp_tp_launches_per_call(int backward, int T);
+
+/* Self-test of the bounded-wait path: launches one small kernel that waits on a barrier
+ * nothing will ever complete, with a limit of `limit_ns` nanoseconds; the wait runs out,
+ * the kernel returns normally, and the next mlp_tp_query_device_status() reports
+ * MLP_ETIMEOUT. The GPU context stays usable. */
+mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLP_TP_H */

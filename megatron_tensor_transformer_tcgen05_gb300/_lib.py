@@ -1,0 +1,127 @@
+"""Thin ctypes binding of libmlp_tp.so (include/mlp_tp.h), same names as the C ABI.
+
+Argument marshalling only: tensors become device pointers, the stream defaults to torch's
+current stream, and a non-OK status raises MlpError. Every step of the block runs in the
+library's CUDA kernels; there is no Python or CPU fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmlp_tp.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "mlp_tp.h")
+
+_lock = threading.Lock()
+_lib = None
+
+_STATUS = {0: "MLP_OK", 1: "MLP_EINVAL", 2: "MLP_ESHAPE", 3: "MLP_EALIGN", 4: "MLP_ECUDA",
+           5: "MLP_ETIMEOUT", 6: "MLP_EUNSUPPORTED", 7: "MLP_EWORKSPACE"}
+STATUS_CODES = {v: k for k, v in _STATUS.items()}
+
+
+class MlpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = _STATUS.get(status, f"status {status}")
+        msg = lib().mlp_tp_status_string(status).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/mlp_tp.h declares."""
+    src = open(HEADER).read()
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mlp_tp_\w+)\s*\(", src, re.M)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmlp_tp.so (built by build.py); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m megatron_tensor_transformer_tcgen05_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_ulonglong
+            L.mlp_tp_forward.restype = i32
+            L.mlp_tp_forward.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 3 + [vp]
+            L.mlp_tp_backward.restype = i32
+            L.mlp_tp_backward.argtypes = [vp] * 6 + [i32] * 4 + [vp] * 5 + [vp, sz, vp]
+            L.mlp_tp_workspace_bytes.restype = sz
+            L.mlp_tp_workspace_bytes.argtypes = [i32] * 4
+            L.mlp_tp_query_device_status.restype = i32
+            L.mlp_tp_query_device_status.argtypes = [vp]
+            L.mlp_tp_last_device_code.restype = i32
+            L.mlp_tp_last_device_code.argtypes = []
+            L.mlp_tp_status_string.restype = ctypes.c_char_p
+            L.mlp_tp_status_string.argtypes = [i32]
+            L.mlp_tp_launches_per_call.restype = i32
+            L.mlp_tp_launches_per_call.argtypes = [i32, i32]
+            L.mlp_tp_selftest_wait_timeout.restype = i32
+            L.mlp_tp_selftest_wait_timeout.argtypes = [u64, vp]
+            _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MlpError(status, where)
+
+
+def mlp_tp_forward(X, A, a, B, b, T: int, h: int, f: int, t: int, H, G, Y, stream=None) -> None:
+    _check(lib().mlp_tp_forward(_ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), T, h, f, t,
+                                _ptr(H), _ptr(G), _ptr(Y), _stream(stream)), "mlp_tp_forward")
+
+
+def mlp_tp_backward(X, A, B, H, G, dY, T: int, h: int, f: int, t: int, dX, dA, dB, da, db,
+                    workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib().mlp_tp_backward(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(G), _ptr(dY), T, h, f, t,
+                                 _ptr(dX), _ptr(dA), _ptr(dB), _ptr(da), _ptr(db), _ptr(workspace),
+                                 workspace_bytes, _stream(stream)), "mlp_tp_backward")
+
+
+def mlp_tp_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
+    return int(lib().mlp_tp_workspace_bytes(T, h, f, t))
+
+
+def mlp_tp_query_device_status(stream=None) -> int:
+    """Returns the raw mlp_status (0 = OK, 5 = a device wait ran out)."""
+    return int(lib().mlp_tp_query_device_status(_stream(stream)))
+
+
+def mlp_tp_last_device_code() -> int:
+    return int(lib().mlp_tp_last_device_code())
+
+
+def mlp_tp_status_string(status: int) -> str:
+    return lib().mlp_tp_status_string(status).decode()
+
+
+def mlp_tp_launches_per_call(backward: bool, T: int) -> int:
+    return int(lib().mlp_tp_launches_per_call(int(bool(backward)), T))
+
+
+def mlp_tp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(lib().mlp_tp_selftest_wait_timeout(limit_ns, _stream(stream)),
+           "mlp_tp_selftest_wait_timeout")

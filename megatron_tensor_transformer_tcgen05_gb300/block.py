@@ -1,0 +1,51 @@
+"""Device buffers and one-call helpers around the C ABI (allocation through PyTorch only).
+
+A user with their own buffers calls the C-ABI names in ``_lib`` directly; these helpers
+allocate the outputs and workspace on the current CUDA device and call the same entry
+points. No arithmetic of the block happens here.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._lib import (mlp_tp_backward, mlp_tp_forward, mlp_tp_workspace_bytes)
+
+
+def empty_buffers(T: int, h: int, f: int, t: int, device="cuda") -> dict[str, torch.Tensor]:
+    """Outputs of one forward + backward, and the backward's workspace."""
+    bf, f32 = torch.bfloat16, torch.float32
+    ws = mlp_tp_workspace_bytes(T, h, f, t)
+    if ws == 0:
+        raise ValueError(f"invalid sizes T={T} h={h} f={f} t={t}")
+    return {
+        "H": torch.empty((T, f), dtype=bf, device=device),
+        "G": torch.empty((T, f), dtype=bf, device=device),
+        "Y": torch.empty((T, h), dtype=bf, device=device),
+        "dX": torch.empty((T, h), dtype=bf, device=device),
+        "dA": torch.empty((h, f), dtype=bf, device=device),
+        "dB": torch.empty((f, h), dtype=bf, device=device),
+        "da": torch.empty((f,), dtype=f32, device=device),
+        "db": torch.empty((h,), dtype=f32, device=device),
+        "ws": torch.empty((ws,), dtype=torch.uint8, device=device),
+    }
+
+
+def forward(inp: dict, buf: dict, t: int, stream=None) -> None:
+    T, h = inp["X"].shape
+    f = inp["A"].shape[1]
+    mlp_tp_forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], T, h, f, t,
+                   buf["H"], buf["G"], buf["Y"], stream)
+
+
+def backward(inp: dict, buf: dict, t: int, stream=None) -> None:
+    T, h = inp["X"].shape
+    f = inp["A"].shape[1]
+    mlp_tp_backward(inp["X"], inp["A"], inp["B"], buf["H"], buf["G"], inp["dY"], T, h, f, t,
+                    buf["dX"], buf["dA"], buf["dB"], buf["da"], buf["db"], buf["ws"],
+                    buf["ws"].numel(), stream)
+
+
+def step(inp: dict, buf: dict, t: int, stream=None) -> None:
+    """One forward + backward of the block."""
+    forward(inp, buf, t, stream)
+    backward(inp, buf, t, stream)

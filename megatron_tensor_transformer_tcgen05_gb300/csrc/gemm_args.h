@@ -1,0 +1,28 @@
+// gemm_args.h -- launch arguments of the tcgen05 GEMM family (host and device view).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mlp {
+
+enum Epi : int { EPI_PLAIN = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2, EPI_DGELU = 3 };
+
+struct GemmArgs {
+    CUtensorMap tmA;    // A operand (K-major box 64x128, or MN-major box 64x64)
+    CUtensorMap tmB;    // B operand (K-major box 64xBN, or MN-major box 64x64)
+    CUtensorMap tmD0;   // first output, store box 32x32, 64B swizzle
+    CUtensorMap tmD1;   // second output (G of EPI_BIAS_GELU), same box
+    int M, N, K;
+    const __nv_bfloat16* bias;   // [N] for EPI_BIAS / EPI_BIAS_GELU
+    const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU
+    long long ld_aux;
+    int* status;                 // device status word (first error code wins)
+    unsigned long long timeout_ns;
+};
+
+// Defined in umma_gemm.cuh; explicitly instantiated once per flavour (gemm_*.cu).
+template <int BN, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
+
+}  // namespace mlp

@@ -1,0 +1,7 @@
+// Backward GEMM 3: dH = (dY*B^T) (.) GELU'(H) (both operands K-major).
+#include "umma_gemm.cuh"
+
+namespace mlp {
+template cudaError_t launch_umma_gemm<128, false, false, EPI_DGELU>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU>(const GemmArgs&, int, cudaStream_t);
+}  // namespace mlp

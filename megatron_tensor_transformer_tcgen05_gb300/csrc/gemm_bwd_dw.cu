@@ -1,0 +1,7 @@
+// Backward GEMMs 5 and 6: dA = X^T*dH and dB = G^T*dY (both operands MN-major).
+#include "umma_gemm.cuh"
+
+namespace mlp {
+template cudaError_t launch_umma_gemm<128, true, true, EPI_PLAIN>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, true, true, EPI_PLAIN>(const GemmArgs&, int, cudaStream_t);
+}  // namespace mlp

@@ -1,0 +1,365 @@
+// mlp_tp_api.cu -- the C ABI of include/mlp_tp.h: argument checks, TMA tensor maps,
+// launch sequencing of the forward (2 kernels) and backward (6 kernels) passes, and the
+// device status word that bounded waits report into.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "colsum.cuh"
+#include "gemm_args.h"
+#include "mlp_tp.h"
+#include "sm103_ptx.cuh"
+
+namespace mlp {
+
+// Device status word: kernels record the first bounded-wait failure here.
+__device__ int g_device_status;
+
+// Limit for every bounded wait inside the GEMMs: one wait never lasts longer than one
+// tile's main loop (well under a millisecond), so two seconds only trips on a real stall.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    int* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+static DeviceInfo g_dev[kMaxDevices];
+static std::mutex g_dev_mu;
+static int g_last_code = 0;
+
+static mlp_status device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLP_ECUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MLP_ECUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MLP_ECUDA;
+        d.status = static_cast<int*>(p);
+        d.ready = true;
+    }
+    if (!d.supported) return MLP_EUNSUPPORTED;
+    *out = &d;
+    return MLP_OK;
+}
+
+// ---- TMA tensor maps -------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [outer, inner]; a box of box_inner x box_outer elements.
+static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand maps: K-major [rows, K] -> box 64 (K) x rows_box; MN-major [K, MN] -> box 64 x 64.
+static bool map_kmajor(CUtensorMap* m, const void* p, uint64_t K, uint64_t rows, uint32_t rows_box)
+{
+    return make_map(m, p, K, rows, 64, rows_box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static bool map_mnmajor(CUtensorMap* m, const void* p, uint64_t MN, uint64_t K)
+{
+    return make_map(m, p, MN, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static bool map_store(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows)
+{
+    return make_map(m, p, cols, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+static int grid_for(int M, int N, int BN, int num_sms)
+{
+    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + BN - 1) / BN);
+    return static_cast<int>(tiles < num_sms ? tiles : num_sms);
+}
+
+// Tile width along N: 256 when the N extent splits into whole 256-wide tiles, else 128.
+static int tile_n(int n) { return (n % 256 == 0) ? 256 : 128; }
+
+template <bool A_MN, bool B_MN, int EPI>
+static cudaError_t gemm(const GemmArgs& g, int BN, int num_sms, cudaStream_t s)
+{
+    const int grid = grid_for(g.M, g.N, BN, num_sms);
+    if (grid <= 0) return cudaSuccess;
+    return BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI>(g, grid, s)
+                     : launch_umma_gemm<128, A_MN, B_MN, EPI>(g, grid, s);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static mlp_status check_shape(int T, int h, int f, int t)
+{
+    if (T < 0 || h < 8 || f < 8 || t < 1) return MLP_EINVAL;
+    if (h % 8 != 0 || f % 8 != 0 || f % t != 0 || (f / t) % 8 != 0) return MLP_ESHAPE;
+    return MLP_OK;
+}
+
+static int colsum_splits(int T)
+{
+    int s = T / 512;
+    return s < 1 ? 1 : (s > 16 ? 16 : s);
+}
+
+static size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+}  // namespace mlp
+
+using namespace mlp;
+
+extern "C" {
+
+const char* mlp_tp_status_string(mlp_status s)
+{
+    switch (s) {
+    case MLP_OK: return "MLP_OK";
+    case MLP_EINVAL: return "MLP_EINVAL: null pointer or non-positive size";
+    case MLP_ESHAPE: return "MLP_ESHAPE: f % t != 0, or h, f, f/t not multiples of 8";
+    case MLP_EALIGN: return "MLP_EALIGN: pointer not 16-byte aligned";
+    case MLP_ECUDA: return "MLP_ECUDA: CUDA runtime error";
+    case MLP_ETIMEOUT: return "MLP_ETIMEOUT: a bounded device wait ran out";
+    case MLP_EUNSUPPORTED: return "MLP_EUNSUPPORTED: current device is not sm_103";
+    case MLP_EWORKSPACE: return "MLP_EWORKSPACE: workspace too small";
+    }
+    return "unknown mlp_status";
+}
+
+size_t mlp_tp_workspace_bytes(int T, int h, int f, int t)
+{
+    if (check_shape(T, h, f, t) != MLP_OK) return 0;
+    const size_t dh = round256(static_cast<size_t>(T) * f * 2);
+    const size_t part = round256(static_cast<size_t>(colsum_splits(T)) * (static_cast<size_t>(f) + h) * 4);
+    return dh + part;
+}
+
+int mlp_tp_launches_per_call(int backward, int T)
+{
+    if (T <= 0) return 0;
+    return backward ? 6 : 2;
+}
+
+mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
+                          const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* G,
+                          mlp_bf16* Y, void* cuda_stream)
+{
+    mlp_status st = check_shape(T, h, f, t);
+    if (st != MLP_OK) return st;
+    // Token-indexed buffers may be NULL only when there are no tokens.
+    if (!A || !a || !B || !b || (T > 0 && (!X || !H || !G || !Y))) return MLP_EINVAL;
+    const void* ptrs[] = {X, A, a, B, b, H, G, Y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    if (T == 0) return MLP_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int fs = f / t;
+    const int bn_f = tile_n(fs), bn_h = tile_n(h);
+
+    // GEMM 1: H = X*A + a, G = GELU(H). N-tiles never straddle a shard when f/t % BN == 0.
+    GemmArgs g1{};
+    if (!map_kmajor(&g1.tmA, X, h, T, 128) || !map_mnmajor(&g1.tmB, A, f, h) ||
+        !map_store(&g1.tmD0, H, f, T) || !map_store(&g1.tmD1, G, f, T))
+        return MLP_ECUDA;
+    g1.M = T; g1.N = f; g1.K = h;
+    g1.bias = reinterpret_cast<const __nv_bfloat16*>(a);
+    g1.status = dev->status;
+    g1.timeout_ns = kWaitLimitNs;
+    if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+
+    // GEMM 2: Y = sum over shards of G_i*B_i, + b. One accumulator over K = f.
+    GemmArgs g2{};
+    if (!map_kmajor(&g2.tmA, G, f, T, 128) || !map_mnmajor(&g2.tmB, B, h, f) ||
+        !map_store(&g2.tmD0, Y, h, T))
+        return MLP_ECUDA;
+    g2.tmD1 = g2.tmD0;
+    g2.M = T; g2.N = h; g2.K = f;
+    g2.bias = reinterpret_cast<const __nv_bfloat16*>(b);
+    g2.status = dev->status;
+    g2.timeout_ns = kWaitLimitNs;
+    if (gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    return MLP_OK;
+}
+
+mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
+                           const mlp_bf16* G, const mlp_bf16* dY, int T, int h, int f, int t,
+                           mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    mlp_status st = check_shape(T, h, f, t);
+    if (st != MLP_OK) return st;
+    // Token-indexed buffers may be NULL only when there are no tokens.
+    if (!A || !B || !dA || !dB || !da || !db || !workspace ||
+        (T > 0 && (!X || !H || !G || !dY || !dX)))
+        return MLP_EINVAL;
+    const void* ptrs[] = {X, A, B, H, G, dY, dX, dA, dB, da, db};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
+    if (workspace_bytes < mlp_tp_workspace_bytes(T, h, f, t)) return MLP_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+    if (T == 0) {  // no tokens: every gradient is an empty sum
+        if (cudaMemsetAsync(dA, 0, static_cast<size_t>(h) * f * 2, s) != cudaSuccess ||
+            cudaMemsetAsync(dB, 0, static_cast<size_t>(f) * h * 2, s) != cudaSuccess ||
+            cudaMemsetAsync(da, 0, static_cast<size_t>(f) * 4, s) != cudaSuccess ||
+            cudaMemsetAsync(db, 0, static_cast<size_t>(h) * 4, s) != cudaSuccess)
+            return MLP_ECUDA;
+        return MLP_OK;
+    }
+    const int fs = f / t;
+    const int bn_f = tile_n(fs), bn_h = tile_n(h);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
+    float* partial = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(T) * f * 2));
+    const int nsplit = colsum_splits(T);
+
+    // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h.
+    GemmArgs g3{};
+    if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, bn_f) ||
+        !map_store(&g3.tmD0, dH, f, T))
+        return MLP_ECUDA;
+    g3.tmD1 = g3.tmD0;
+    g3.M = T; g3.N = f; g3.K = h;
+    g3.aux = reinterpret_cast<const __nv_bfloat16*>(H);
+    g3.ld_aux = f;
+    g3.status = dev->status;
+    g3.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+
+    // GEMM 4: dX = sum over shards of dH_i*A_i^T; A [h,f] is K-major for N = h, K = f.
+    GemmArgs g4{};
+    if (!map_kmajor(&g4.tmA, dH, f, T, 128) || !map_kmajor(&g4.tmB, A, f, h, bn_h) ||
+        !map_store(&g4.tmD0, dX, h, T))
+        return MLP_ECUDA;
+    g4.tmD1 = g4.tmD0;
+    g4.M = T; g4.N = h; g4.K = f;
+    g4.status = dev->status;
+    g4.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+
+    // GEMM 5: dA = X^T*dH (M = h, N = f, K = T), both operands MN-major.
+    GemmArgs g5{};
+    if (!map_mnmajor(&g5.tmA, X, h, T) || !map_mnmajor(&g5.tmB, dH, f, T) ||
+        !map_store(&g5.tmD0, dA, f, h))
+        return MLP_ECUDA;
+    g5.tmD1 = g5.tmD0;
+    g5.M = h; g5.N = f; g5.K = T;
+    g5.status = dev->status;
+    g5.timeout_ns = kWaitLimitNs;
+    if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+
+    // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major.
+    GemmArgs g6{};
+    if (!map_mnmajor(&g6.tmA, G, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) ||
+        !map_store(&g6.tmD0, dB, h, f))
+        return MLP_ECUDA;
+    g6.tmD1 = g6.tmD0;
+    g6.M = f; g6.N = h; g6.K = T;
+    g6.status = dev->status;
+    g6.timeout_ns = kWaitLimitNs;
+    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+
+    // Bias gradients: da = colsum(dH), db = colsum(dY), two passes, fixed order.
+    const int strips = (f + kColsumStrip - 1) / kColsumStrip + (h + kColsumStrip - 1) / kColsumStrip;
+    colsum_partial_kernel<<<dim3(strips, nsplit), kColsumThreads, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(dH), f, reinterpret_cast<const __nv_bfloat16*>(dY), h,
+        T, nsplit, partial);
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    return MLP_OK;
+}
+
+mlp_status mlp_tp_query_device_status(void* cuda_stream)
+{
+    DeviceInfo* dev = nullptr;
+    mlp_status st = device_info(&dev);
+    if (st != MLP_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return MLP_ECUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MLP_ECUDA;
+    if (v != 0) {
+        g_last_code = v;
+        const int zero = 0;
+        if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return MLP_ECUDA;
+        return MLP_ETIMEOUT;
+    }
+    return MLP_OK;
+}
+
+int mlp_tp_last_device_code(void) { return g_last_code; }
+
+}  // extern "C"
+
+namespace mlp {
+
+// Waits on a barrier whose phase nothing completes; the bounded wait must give up.
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, limit_ns, DEV_TIMEOUT_SELFTEST);
+}
+
+}  // namespace mlp
+
+extern "C" mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, void* cuda_stream)
+{
+    DeviceInfo* dev = nullptr;
+    mlp_status st = device_info(&dev);
+    if (st != MLP_OK) return st;
+    if (limit_ns > 10000000000ull) return MLP_EINVAL;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(dev->status, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? MLP_OK : MLP_ECUDA;
+}

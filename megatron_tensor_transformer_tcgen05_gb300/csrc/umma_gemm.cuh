@@ -1,0 +1,401 @@
+// umma_gemm.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with fused
+// epilogues for the tensor-parallel MLP block.
+//
+//   D[M,N] = sum_k  Aop[m,k] * Bop[n,k]      (bf16 operands, fp32 accumulation in TMEM)
+//
+// Aop and Bop are read from row-major global tensors through TMA tensor maps, either
+// K-contiguous ("K-major") or M/N-contiguous ("MN-major", i.e. the transposed use of a
+// row-major tensor); the tcgen05 instruction descriptor carries the major-ness, so no
+// operand is ever transposed in memory.
+//
+// Roles in one CTA (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer: fills a 4-stage ring of {A 128x64, B BNx64} tiles (128B swizzle)
+//   warp 1     allocates TMEM (two BN-column fp32 accumulators) and issues tcgen05.mma
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused element-wise math, bf16 RNE,
+//              swizzled staging in shared memory, TMA store of 32x32 boxes
+// The two accumulators let the epilogue of tile i overlap the main loop of tile i+1.
+//
+// Epilogues (the step of the MLP block each one implements):
+//   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H)            -> stores H and G
+//   EPI_BIAS       Y = acc + b[n]                          -> stores Y
+//   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH
+//   EPI_PLAIN      D = acc                                 -> stores D
+// GELU is the tanh form 0.5 x (1 + tanh u), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated
+// through the identity 1 + tanh u = 2 / (1 + exp(-2u)), which stays accurate where
+// 1 + tanh u is small.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "gemm_args.h"
+#include "sm103_ptx.cuh"
+
+namespace mlp {
+
+template <int BN_, bool A_MN_, bool B_MN_, int EPI_>
+struct GemmCfg {
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = 4, UMMA_K = 16;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
+    static constexpr int EPI = EPI_;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int NOUT = (EPI == EPI_BIAS_GELU) ? 2 : 1;
+    static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
+    static constexpr uint32_t EPI_BYTES = 4 * 2 * NOUT * STG_BYTES;  // 4 warps x 2 buffers
+    static constexpr uint32_t TMEM_COLS = 2 * BN;                    // two fp32 accumulators
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr uint32_t BAR_BYTES = 8 * NUM_BARS + 16;
+    static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int THREADS = 192;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// In-flight copies get this long to land after an abort before the CTA exits.
+constexpr unsigned long long kDrainLimitNs = 2000000000ull;
+
+__device__ __forceinline__ float gelu_tanh_f(float x)
+{
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float u = k0 * x * fmaf(k1, x * x, 1.0f);
+    const float e = __expf(-2.0f * u);
+    return x * __fdividef(1.0f, 1.0f + e);  // x * sigmoid(2u)
+}
+
+// d/dx of the tanh form with s = sigmoid(2u): 1 + tanh u = 2s and 1 - tanh^2 u = 4 s (1 - s),
+// so GELU'(x) = s + 2 x s (1 - s) u'(x), u'(x) = sqrt(2/pi) (1 + 3 * 0.044715 x^2).
+__device__ __forceinline__ float gelu_tanh_grad_f(float x)
+{
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float x2 = x * x;
+    const float u = k0 * x * fmaf(k1, x2, 1.0f);
+    const float e = __expf(-2.0f * u);
+    const float s = __fdividef(1.0f, 1.0f + e);
+    const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
+    return fmaf(2.0f * x * s * (1.0f - s), du, s);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* out)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Write one thread's 32 bf16 (16 packed words) as row `lane` of a 32x32 box laid out the
+// way a 64-byte-swizzled TMA store reads it: 16-byte chunk j of row r sits at chunk
+// j ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_row_sw64(uint32_t buf, int lane, const uint32_t (&p)[16])
+{
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 64u;
+    const uint32_t x = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j)
+        sts_v4(row + ((j ^ x) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
+{
+    using C = GemmCfg<BN, A_MN, B_MN, EPI>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t s_stages = base;
+    const uint32_t s_epi = base + C::STAGES * C::STAGE_BYTES;
+    const uint32_t s_bar = s_epi + C::EPI_BYTES;
+    // barrier map: full[S] | empty[S] | acc_full[2] | acc_empty[2] | drain | tmem slot | abort
+    const uint32_t b_full = s_bar, b_empty = s_bar + 8u * C::STAGES;
+    const uint32_t b_accf = s_bar + 16u * C::STAGES, b_acce = b_accf + 16u;
+    const uint32_t b_drain = b_acce + 16u;
+    const uint32_t s_slot = b_drain + 8u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (s_slot - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (s_slot + 4u - base));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = args.M, N = args.N, K = args.K;
+    const int tiles_m = (M + C::BM - 1) / C::BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int num_kb = (K + C::BK - 1) / C::BK;
+    const unsigned long long limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(b_full + 8u * s, 1);
+            mbar_init(b_empty + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(b_accf + 8u * a, 1);
+            mbar_init(b_acce + 8u * a, 4);  // one arrive per epilogue warp
+        }
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&args.tmA);
+        tma_prefetch_desc(&args.tmB);
+        tma_prefetch_desc(&args.tmD0);
+        if (C::NOUT == 2) tma_prefetch_desc(&args.tmD1);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0, par = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile % tiles_m) * C::BM;
+                const int n0 = (tile / tiles_m) * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_bounded(b_empty + 8u * stage, phase ^ 1u, abort_flag, args.status,
+                                           limit, DEV_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = s_stages + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
+                    const uint32_t fb = b_full + 8u * stage;
+                    const int k0 = kb * C::BK;
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    if (A_MN) {
+                        tma_load_2d(sa, &args.tmA, m0, k0, fb);
+                        tma_load_2d(sa + 8192u, &args.tmA, m0 + 64, k0, fb);
+                    } else {
+                        tma_load_2d(sa, &args.tmA, k0, m0, fb);
+                    }
+                    if (B_MN) {
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_2d(sb + 8192u * i, &args.tmB, n0 + 64 * i, k0, fb);
+                    } else {
+                        tma_load_2d(sb, &args.tmB, k0, n0, fb);
+                    }
+                    issued |= 1u << stage;
+                    par = (par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy this thread started land before the CTA may exit.
+                volatile int never = 0;
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued & (1u << s))
+                        mbar_wait_bounded(b_full + 8u * s, (par >> s) & 1u, &never, args.status,
+                                          kDrainLimitNs, DEV_TIMEOUT_DRAIN);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true, any = false;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!mbar_wait_bounded(b_acce + 8u * acc, acc_phase ^ 1u, abort_flag, args.status,
+                                       limit, DEV_TIMEOUT_MMA_ACC)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_bounded(b_full + 8u * stage, phase, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = s_stages + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
+                        // K-major: next 16 elements are 32 bytes further along the swizzled row.
+                        // MN-major: next 16 k-rows are two 8-row (1024-byte) groups further.
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                                 : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                                 : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+                        umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    any = true;
+                    umma_commit(b_empty + 8u * stage);  // stage is free once these MMAs finish
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(b_accf + 8u * acc);  // accumulator ready for the epilogue
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && any) {
+                // Let the MMAs already issued finish before TMEM is released.
+                volatile int never = 0;
+                umma_commit(b_drain);
+                mbar_wait_bounded(b_drain, 0, &never, args.status, kDrainLimitNs, DEV_TIMEOUT_DRAIN);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue ----------------------------------
+        const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the ones this warp may read
+        uint32_t acc = 0, acc_phase = 0, sel = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            // One lane waits; the warp follows its verdict so the .sync.aligned TMEM loads
+            // below always run with all 32 lanes.
+            int ready = 0;
+            if (lane == 0)
+                ready = mbar_wait_bounded(b_accf + 8u * acc, acc_phase, abort_flag, args.status, limit,
+                                          DEV_TIMEOUT_EPILOGUE);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) break;
+            tc_fence_after();
+            const int m0 = (tile % tiles_m) * C::BM;
+            const int n0 = (tile / tiles_m) * BN;
+            const int row_blk = m0 + 32 * q;
+            const int row = row_blk + lane;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+
+            uint4 hnext[4];
+            if (EPI == EPI_DGELU) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int n = n0 + 8 * i;
+                    hnext[i] = (row < M && n < N)
+                                   ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
+                                   : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int nc = n0 + 32 * c;
+                const bool active = nc < N;  // warp-uniform
+                uint32_t r[32];
+                if (active) {
+                    tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                    tmem_ld_wait();
+                }
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_acce + 8u * acc);  // accumulator may be reused
+                }
+                if (!active || row_blk >= M) continue;
+
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                uint32_t p0[16], p1[16];
+                if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float bv[8];
+                        const int n = nc + 8 * i;
+                        const uint4 u = n < N ? ldg_nc_v4(args.bias + n) : make_uint4(0, 0, 0, 0);
+                        unpack_bf16x8(u, bv);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * i + j] += bv[j];
+                    }
+                }
+                if (EPI == EPI_DGELU) {
+                    float hv[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
+                    if (c + 1 < BN / 32) {  // prefetch the next chunk of H
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int n = nc + 32 + 8 * i;
+                            hnext[i] = (row < M && n < N)
+                                           ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
+                                           : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(hv[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                if (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        p1[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]), gelu_tanh_f(v[2 * j + 1]));
+                }
+
+                const uint32_t buf0 = s_epi + ((q * 2 + sel) * C::NOUT) * C::STG_BYTES;
+                if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `sel` has read it
+                __syncwarp();
+                stage_row_sw64(buf0, lane, p0);
+                if (EPI == EPI_BIAS_GELU) stage_row_sw64(buf0 + C::STG_BYTES, lane, p1);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&args.tmD0, nc, row_blk, buf0);
+                    if (EPI == EPI_BIAS_GELU) tma_store_2d(&args.tmD1, nc, row_blk, buf0 + C::STG_BYTES);
+                    bulk_commit_group();
+                }
+                sel ^= 1u;
+            }
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait_group<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// Host-side launcher, instantiated once per GEMM flavour in its own translation unit.
+template <int BN, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream)
+{
+    using C = GemmCfg<BN, A_MN, B_MN, EPI>;
+    auto kern = umma_gemm_kernel<BN, A_MN, B_MN, EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace mlp

@@ -1,0 +1,81 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads without a GPU,
+exports every function the header declares, and rejects bad arguments before it touches
+the GPU (these calls fail in argument checking, so they never reach CUDA)."""
+import ctypes
+
+import pytest
+
+from megatron_tensor_transformer_tcgen05_gb300 import build as build_mod
+from megatron_tensor_transformer_tcgen05_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return _lib.lib()
+
+
+def test_header_symbols_exported(L):
+    names = _lib.header_functions()
+    assert {"mlp_tp_forward", "mlp_tp_backward", "mlp_tp_workspace_bytes",
+            "mlp_tp_query_device_status", "mlp_tp_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/mlp_tp.h but not exported"
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = _lib.mlp_tp_status_string(code)
+        assert s.startswith(_lib._STATUS[code])
+    assert "unknown" in _lib.mlp_tp_status_string(99)
+
+
+def test_workspace_bytes():
+    assert _lib.mlp_tp_workspace_bytes(128, 64, 256, 2) >= 128 * 256 * 2
+    assert _lib.mlp_tp_workspace_bytes(128, 64, 256, 3) == 0      # f % t
+    assert _lib.mlp_tp_workspace_bytes(128, 60, 256, 2) == 0      # h % 8
+    assert _lib.mlp_tp_workspace_bytes(-1, 64, 256, 2) == 0
+    assert _lib.mlp_tp_workspace_bytes(0, 64, 256, 2) > 0         # partials only
+
+
+def test_launch_counts():
+    assert _lib.mlp_tp_launches_per_call(False, 128) == 2
+    assert _lib.mlp_tp_launches_per_call(True, 128) == 6
+    assert _lib.mlp_tp_launches_per_call(True, 0) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails its checks
+
+
+@pytest.mark.parametrize("T,h,f,t,code", [
+    (128, 64, 256, 3, "MLP_ESHAPE"),   # f % t != 0
+    (128, 60, 256, 2, "MLP_ESHAPE"),   # h % 8 != 0
+    (128, 64, 256, 64, "MLP_ESHAPE"),  # f/t = 4, not a multiple of 8
+    (128, 64, 256, 0, "MLP_EINVAL"),
+    (-1, 64, 256, 2, "MLP_EINVAL"),
+    (128, 0, 256, 2, "MLP_EINVAL"),
+])
+def test_forward_rejects_bad_shapes(L, T, h, f, t, code):
+    st = L.mlp_tp_forward(*([FAKE] * 5), T, h, f, t, FAKE, FAKE, FAKE, None)
+    assert st == _lib.STATUS_CODES[code]
+
+
+def test_forward_rejects_null_and_misaligned(L):
+    assert L.mlp_tp_forward(None, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None) == 1
+    assert L.mlp_tp_forward(FAKE + 8, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None) == 3
+
+
+def test_backward_rejects_bad_arguments(L):
+    args = [FAKE] * 6 + [128, 64, 256, 2] + [FAKE] * 5
+    ws = _lib.mlp_tp_workspace_bytes(128, 64, 256, 2)
+    assert L.mlp_tp_backward(*args, FAKE, ws - 256, None) == _lib.STATUS_CODES["MLP_EWORKSPACE"]
+    assert L.mlp_tp_backward(*args, FAKE + 16, ws, None) == _lib.STATUS_CODES["MLP_EALIGN"]
+    assert L.mlp_tp_backward(*args, None, ws, None) == _lib.STATUS_CODES["MLP_EINVAL"]
+    bad = [FAKE] * 6 + [128, 64, 256, 3] + [FAKE] * 5
+    assert L.mlp_tp_backward(*bad, FAKE, ws, None) == _lib.STATUS_CODES["MLP_ESHAPE"]
+
+
+def test_binding_raises_named_error(L):
+    with pytest.raises(_lib.MlpError) as ei:
+        _lib.mlp_tp_forward(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 64, 256, 3, FAKE, FAKE, FAKE, stream=0)
+    assert ei.value.name == "MLP_ESHAPE"
