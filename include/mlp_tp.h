@@ -106,6 +106,26 @@ int mlp_tp_launches_per_call(int backward, int T);
  * MLP_ETIMEOUT. The GPU context stays usable. */
 mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, void* cuda_stream);
 
+/* Per-kernel timing for benchmarks. While enabled, every forward/backward call records a
+ * CUDA event on its stream before its first launch and after each launch (no extra
+ * synchronisation). mlp_tp_timing_collect() waits for those events, writes the summed
+ * milliseconds and launch counts per kernel id into ms[MLP_NUM_KERNELS] and
+ * counts[MLP_NUM_KERNELS], and forgets them. */
+enum {
+    MLP_K_FWD_UP = 0,        /* H = X*A + a, G = GELU(H) */
+    MLP_K_FWD_DOWN = 1,      /* Y = G*B + b */
+    MLP_K_BWD_DH = 2,        /* dH = (dY*B^T) (.) GELU'(H) */
+    MLP_K_BWD_DX = 3,        /* dX = dH*A^T */
+    MLP_K_BWD_DA = 4,        /* dA = X^T*dH */
+    MLP_K_BWD_DB = 5,        /* dB = G^T*dY */
+    MLP_K_COLSUM_PARTIAL = 6,/* da, db partial column sums */
+    MLP_K_COLSUM_FINAL = 7,  /* da, db final sums */
+    MLP_NUM_KERNELS = 8
+};
+mlp_status mlp_tp_timing_enable(int on);
+mlp_status mlp_tp_timing_collect(double* ms, int* counts);
+const char* mlp_tp_kernel_name(int kernel);
+
 #ifdef __cplusplus
 }
 #endif

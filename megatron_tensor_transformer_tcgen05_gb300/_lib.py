@@ -63,6 +63,12 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_launches_per_call.argtypes = [i32, i32]
             L.mlp_tp_selftest_wait_timeout.restype = i32
             L.mlp_tp_selftest_wait_timeout.argtypes = [u64, vp]
+            L.mlp_tp_timing_enable.restype = i32
+            L.mlp_tp_timing_enable.argtypes = [i32]
+            L.mlp_tp_timing_collect.restype = i32
+            L.mlp_tp_timing_collect.argtypes = [vp, vp]
+            L.mlp_tp_kernel_name.restype = ctypes.c_char_p
+            L.mlp_tp_kernel_name.argtypes = [i32]
             _lib = L
     return _lib
 
@@ -125,3 +131,21 @@ def mlp_tp_launches_per_call(backward: bool, T: int) -> int:
 def mlp_tp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(lib().mlp_tp_selftest_wait_timeout(limit_ns, _stream(stream)),
            "mlp_tp_selftest_wait_timeout")
+
+
+MLP_NUM_KERNELS = 8
+
+
+def mlp_tp_timing_enable(on: bool) -> None:
+    _check(lib().mlp_tp_timing_enable(int(bool(on))), "mlp_tp_timing_enable")
+
+
+def mlp_tp_timing_collect() -> tuple[list[float], list[int]]:
+    ms = (ctypes.c_double * MLP_NUM_KERNELS)()
+    counts = (ctypes.c_int * MLP_NUM_KERNELS)()
+    _check(lib().mlp_tp_timing_collect(ms, counts), "mlp_tp_timing_collect")
+    return list(ms), list(counts)
+
+
+def mlp_tp_kernel_name(kernel: int) -> str:
+    return lib().mlp_tp_kernel_name(kernel).decode()

@@ -4,8 +4,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "colsum.cuh"
 #include "gemm_args.h"
@@ -143,6 +145,61 @@ static int colsum_splits(int T)
 
 static size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
+// ---- optional per-kernel timing (benchmarks) ---------------------------------------------
+// When enabled, each call records a CUDA event on its stream before its first launch and
+// after every launch; mlp_tp_timing_collect() turns the pairs into per-kernel milliseconds.
+
+struct TimingMark {
+    int kernel;
+    cudaEvent_t start, stop;
+};
+static std::mutex g_tm_mu;
+static bool g_timing = false;
+static std::vector<TimingMark> g_marks;
+static std::vector<cudaEvent_t> g_event_pool;
+
+static cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+class CallTimer {
+  public:
+    explicit CallTimer(cudaStream_t s) : s_(s)
+    {
+        std::lock_guard<std::mutex> lk(g_tm_mu);
+        on_ = g_timing;
+        if (on_) {
+            prev_ = take_event();
+            on_ = prev_ != nullptr && cudaEventRecord(prev_, s_) == cudaSuccess;
+        }
+    }
+    void mark(int kernel)
+    {
+        if (!on_) return;
+        std::lock_guard<std::mutex> lk(g_tm_mu);
+        cudaEvent_t e = take_event();
+        if (!e || cudaEventRecord(e, s_) != cudaSuccess) {
+            on_ = false;
+            return;
+        }
+        g_marks.push_back({kernel, prev_, e});
+        prev_ = e;
+    }
+
+  private:
+    cudaStream_t s_;
+    bool on_ = false;
+    cudaEvent_t prev_ = nullptr;
+};
+
 }  // namespace mlp
 
 using namespace mlp;
@@ -195,6 +252,7 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int fs = f / t;
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
+    CallTimer timer(s);
 
     // GEMM 1: H = X*A + a, G = GELU(H). N-tiles never straddle a shard when f/t % BN == 0.
     GemmArgs g1{};
@@ -206,6 +264,7 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
     g1.status = dev->status;
     g1.timeout_ns = kWaitLimitNs;
     if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_FWD_UP);
 
     // GEMM 2: Y = sum over shards of G_i*B_i, + b. One accumulator over K = f.
     GemmArgs g2{};
@@ -218,6 +277,7 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
     g2.status = dev->status;
     g2.timeout_ns = kWaitLimitNs;
     if (gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_FWD_DOWN);
     return MLP_OK;
 }
 
@@ -255,6 +315,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
     float* partial = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(T) * f * 2));
     const int nsplit = colsum_splits(T);
+    CallTimer timer(s);
 
     // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h.
     GemmArgs g3{};
@@ -268,6 +329,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
     if (gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DH);
 
     // GEMM 4: dX = sum over shards of dH_i*A_i^T; A [h,f] is K-major for N = h, K = f.
     GemmArgs g4{};
@@ -279,6 +341,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     g4.status = dev->status;
     g4.timeout_ns = kWaitLimitNs;
     if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DX);
 
     // GEMM 5: dA = X^T*dH (M = h, N = f, K = T), both operands MN-major.
     GemmArgs g5{};
@@ -290,6 +353,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     g5.status = dev->status;
     g5.timeout_ns = kWaitLimitNs;
     if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DA);
 
     // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major.
     GemmArgs g6{};
@@ -301,6 +365,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     g6.status = dev->status;
     g6.timeout_ns = kWaitLimitNs;
     if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DB);
 
     // Bias gradients: da = colsum(dH), db = colsum(dY), two passes, fixed order.
     const int strips = (f + kColsumStrip - 1) / kColsumStrip + (h + kColsumStrip - 1) / kColsumStrip;
@@ -308,8 +373,10 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
         reinterpret_cast<const __nv_bfloat16*>(dH), f, reinterpret_cast<const __nv_bfloat16*>(dY), h,
         T, nsplit, partial);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_COLSUM_PARTIAL);
     colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_COLSUM_FINAL);
     return MLP_OK;
 }
 
@@ -332,6 +399,54 @@ mlp_status mlp_tp_query_device_status(void* cuda_stream)
 }
 
 int mlp_tp_last_device_code(void) { return g_last_code; }
+
+mlp_status mlp_tp_timing_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    g_timing = on != 0;
+    return MLP_OK;
+}
+
+mlp_status mlp_tp_timing_collect(double* ms, int* counts)
+{
+    if (!ms || !counts) return MLP_EINVAL;
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    for (int k = 0; k < MLP_NUM_KERNELS; ++k) {
+        ms[k] = 0.0;
+        counts[k] = 0;
+    }
+    mlp_status st = MLP_OK;
+    for (const TimingMark& m : g_marks) {
+        float t = 0.f;
+        if (cudaEventSynchronize(m.stop) != cudaSuccess || cudaEventElapsedTime(&t, m.start, m.stop) != cudaSuccess)
+            st = MLP_ECUDA;
+        if (m.kernel >= 0 && m.kernel < MLP_NUM_KERNELS) {
+            ms[m.kernel] += t;
+            counts[m.kernel] += 1;
+        }
+    }
+    // Every event appears once as a stop; starts are either a previous stop or a call's
+    // first event, which is never a stop. Return each exactly once to the pool.
+    std::vector<cudaEvent_t> seen;
+    for (const TimingMark& m : g_marks) {
+        seen.push_back(m.start);
+        seen.push_back(m.stop);
+    }
+    std::sort(seen.begin(), seen.end());
+    seen.erase(std::unique(seen.begin(), seen.end()), seen.end());
+    for (cudaEvent_t e : seen) g_event_pool.push_back(e);
+    g_marks.clear();
+    return st;
+}
+
+const char* mlp_tp_kernel_name(int kernel)
+{
+    static const char* names[MLP_NUM_KERNELS] = {
+        "gemm_fwd_up (H=XA+a, G=GELU(H))", "gemm_fwd_down (Y=GB+b)", "gemm_bwd_dh (dH=dY B^T * GELU'(H))",
+        "gemm_bwd_dx (dX=dH A^T)",          "gemm_bwd_da (dA=X^T dH)", "gemm_bwd_db (dB=G^T dY)",
+        "colsum_partial (da, db)",          "colsum_finalize (da, db)"};
+    return (kernel >= 0 && kernel < MLP_NUM_KERNELS) ? names[kernel] : "unknown";
+}
 
 }  // extern "C"
 
