@@ -76,12 +76,32 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
  *   dA = X^T*dH,  dB = G^T*dY         local weight gradients
  *   da = colsum(dH) (fp32),  db = colsum(dY) (fp32)
  * `workspace` (device, >= mlp_tp_workspace_bytes(T,h,f,t) bytes, 256-byte aligned) holds
- * dH and the reduction partials; its contents on entry do not matter. Six launches. */
+ * dH and the reduction partials; its contents on entry do not matter. On return its first
+ * T*f*2 bytes hold dH = dL/dH (row-major bf16 [T,f]). Six launches. */
 mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
                            const mlp_bf16* H, const mlp_bf16* G, const mlp_bf16* dY,
                            int T, int h, int f, int t,
                            mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
                            void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Bias gradients da = colsum(dH), db = colsum(dY) (fp32, same kernels and results as
+ * mlp_tp_backward's) with no workspace and no device allocation of any kind. The paper has
+ * no counterpart to this entry point; it exists for callers that cannot allocate device
+ * memory when they need these sums: code running inside another runtime that owns all
+ * device memory (a framework allocator or fixed arena with nothing to lend), and
+ * latency-bound loops where a cudaMalloc would synchronise the device.
+ * The partial sums live in one fixed device array inside the library (4 MiB per GPU, held
+ * from library load until process exit): sizes with clamp(T/512, 1, 16) * (f + h) > 2^20
+ * are rejected with MLP_EWORKSPACE before anything is launched. The first call on a device
+ * looks up that array's device address (one cudaGetSymbolAddress, with the device
+ * current); make that first call outside any stream capture. Every call on a device
+ * shares the one array: calls that can overlap on the GPU (different streams without
+ * ordering between them) race and give wrong sums, so order them. Each call rewrites every
+ * partial it later reads, so stale contents from an earlier call are harmless.
+ * dH [T,f], dY [T,h] row-major bf16 (may be NULL when T == 0); da [f], db [h] fp32; all
+ * 16-byte aligned; h, f >= 8 and multiples of 8. Asynchronous on cuda_stream. */
+mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf16* dY, int T, int h, int f,
+                                     float* da, float* db, void* cuda_stream);
 
 /* Device bytes mlp_tp_backward needs as workspace for these sizes (0 on invalid sizes). */
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);

@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_timing_collect.argtypes = [vp, vp]
             L.mlp_tp_kernel_name.restype = ctypes.c_char_p
             L.mlp_tp_kernel_name.argtypes = [i32]
+            L.mlp_tp_bias_grads_noalloc.restype = i32
+            L.mlp_tp_bias_grads_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -149,3 +151,10 @@ def mlp_tp_timing_collect() -> tuple[list[float], list[int]]:
 
 def mlp_tp_kernel_name(kernel: int) -> str:
     return lib().mlp_tp_kernel_name(kernel).decode()
+
+
+def mlp_tp_bias_grads_noalloc(dH, dY, T: int, h: int, f: int, da, db, stream=None) -> None:
+    """da = colsum(dH), db = colsum(dY) with no workspace: the library's fixed device
+    scratch array holds the partial sums (see include/mlp_tp.h for its limit)."""
+    _check(lib().mlp_tp_bias_grads_noalloc(_ptr(dH), _ptr(dY), T, h, f, _ptr(da), _ptr(db),
+                                           _stream(stream)), "mlp_tp_bias_grads_noalloc")

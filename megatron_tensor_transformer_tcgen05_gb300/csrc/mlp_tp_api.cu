@@ -478,3 +478,69 @@ extern "C" mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, 
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(dev->status, limit_ns);
     return cudaGetLastError() == cudaSuccess ? MLP_OK : MLP_ECUDA;
 }
+
+// ---- bias gradients with no device allocation --------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they need the bias
+// gradients: code embedded in another runtime that owns all device memory (a framework's
+// caching allocator or a fixed arena with no room to lend a workspace), and latency-bound
+// loops where a cudaMalloc would synchronise the device. For them this entry point keeps
+// the reduction's partial sums in a fixed, file-scope device array instead of a caller
+// workspace. The array is loaded with the library and stays resident on every GPU that
+// loads it until the process exits.
+
+namespace mlp {
+
+// Room for the partial sums of slices x (f + h) columns: 2^20 floats = 4 MiB per GPU.
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+static float* g_noalloc_ptr[kMaxDevices];
+static std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+// (In host code the array's name is only a host-side stand-in, never a device address.)
+static mlp_status noalloc_scratch(float** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLP_ECUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLP_ECUDA;
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MLP_OK;
+}
+
+}  // namespace mlp
+
+extern "C" mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf16* dY, int T, int h, int f,
+                                                float* da, float* db, void* cuda_stream)
+{
+    mlp_status st = check_shape(T, h, f, 1);
+    if (st != MLP_OK) return st;
+    if (!da || !db || (T > 0 && (!dH || !dY))) return MLP_EINVAL;
+    const void* ptrs[] = {dH, dY, da, db};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    const int nsplit = colsum_splits(T);
+    if (static_cast<size_t>(nsplit) * (static_cast<size_t>(f) + h) > kNoAllocScratchFloats)
+        return MLP_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    float* partial = nullptr;
+    if ((st = noalloc_scratch(&partial)) != MLP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    // Every slice row of the partial array is written by the first kernel before the second
+    // reads it, so nothing left from an earlier call is ever read and no clearing is needed.
+    const int strips = (f + kColsumStrip - 1) / kColsumStrip + (h + kColsumStrip - 1) / kColsumStrip;
+    colsum_partial_kernel<<<dim3(strips, nsplit), kColsumThreads, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(dH), f, reinterpret_cast<const __nv_bfloat16*>(dY), h, T,
+        nsplit, partial);
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    return MLP_OK;
+}
