@@ -14,6 +14,7 @@ struct GemmArgs {
     CUtensorMap tmD0;   // first output, store box 32x32, 64B swizzle
     CUtensorMap tmD1;   // second output (G of EPI_BIAS_GELU), same box
     int M, N, K;
+    int n_fastest;               // tile order: 0 = M index fastest, 1 = N index fastest
     const __nv_bfloat16* bias;   // [N] for EPI_BIAS / EPI_BIAS_GELU
     const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU
     long long ld_aux;

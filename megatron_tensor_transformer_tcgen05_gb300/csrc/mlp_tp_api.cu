@@ -120,8 +120,12 @@ static int grid_for(int M, int N, int BN, int num_sms)
 static int tile_n(int n) { return (n % 256 == 0) ? 256 : 128; }
 
 template <bool A_MN, bool B_MN, int EPI>
-static cudaError_t gemm(const GemmArgs& g, int BN, int num_sms, cudaStream_t s)
+static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
 {
+    // Keep the smaller operand resident in L2 and stream the larger one once: with A
+    // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
+    // B block; otherwise sweep N fastest so they share one A block.
+    g.n_fastest = g.M > g.N ? 1 : 0;
     const int grid = grid_for(g.M, g.N, BN, num_sms);
     if (grid <= 0) return cudaSuccess;
     return BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI>(g, grid, s)

@@ -121,6 +121,21 @@ __device__ __forceinline__ void stage_row_sw64(uint32_t buf, int lane, const uin
         sts_v4(row + ((j ^ x) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
 }
 
+// Output tile `tile` -> its first row and column. Consecutive tiles run at the same time on
+// neighbouring SMs, so the index that varies fastest decides which operand they share
+// through L2: M-fastest tiles share one B block and stream A, N-fastest share one A block.
+__device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, int n_fastest, int BN,
+                                            int& m0, int& n0)
+{
+    if (n_fastest) {
+        m0 = (tile / tiles_n) * 128;
+        n0 = (tile % tiles_n) * BN;
+    } else {
+        m0 = (tile % tiles_m) * 128;
+        n0 = (tile / tiles_m) * BN;
+    }
+}
+
 template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
 {
@@ -180,8 +195,8 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0, issued = 0, par = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % tiles_m) * C::BM;
-                const int n0 = (tile / tiles_m) * BN;
+                int m0, n0;
+                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, BN, m0, n0);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_bounded(b_empty + 8u * stage, phase ^ 1u, abort_flag, args.status,
                                            limit, DEV_TIMEOUT_PRODUCER)) {
@@ -288,8 +303,8 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             ready = __shfl_sync(0xffffffffu, ready, 0);
             if (!ready) break;
             tc_fence_after();
-            const int m0 = (tile % tiles_m) * C::BM;
-            const int n0 = (tile / tiles_m) * BN;
+            int m0, n0;
+            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, BN, m0, n0);
             const int row_blk = m0 + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
