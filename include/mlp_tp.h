@@ -114,6 +114,10 @@ mlp_status mlp_tp_query_device_status(void* cuda_stream);
 /* The raw device status code behind the last MLP_ETIMEOUT (which wait gave up), or 0. */
 int mlp_tp_last_device_code(void);
 
+/* Where the bounded wait behind the last MLP_ETIMEOUT gave up: block index, thread index,
+ * output tile and k block (-1 where not applicable). Returns the device code, or 0. */
+int mlp_tp_last_device_where(int* block, int* thread, int* tile, int* kblock);
+
 /* Human-readable name of a status. Never NULL. */
 const char* mlp_tp_status_string(mlp_status s);
 

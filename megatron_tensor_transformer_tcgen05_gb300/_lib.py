@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_query_device_status.argtypes = [vp]
             L.mlp_tp_last_device_code.restype = i32
             L.mlp_tp_last_device_code.argtypes = []
+            L.mlp_tp_last_device_where.restype = i32
+            L.mlp_tp_last_device_where.argtypes = [vp, vp, vp, vp]
             L.mlp_tp_status_string.restype = ctypes.c_char_p
             L.mlp_tp_status_string.argtypes = [i32]
             L.mlp_tp_launches_per_call.restype = i32
@@ -120,6 +122,14 @@ def mlp_tp_query_device_status(stream=None) -> int:
 
 def mlp_tp_last_device_code() -> int:
     return int(lib().mlp_tp_last_device_code())
+
+
+def mlp_tp_last_device_where() -> dict:
+    """Where the bounded wait behind the last MLP_ETIMEOUT gave up."""
+    v = [ctypes.c_int() for _ in range(4)]
+    code = lib().mlp_tp_last_device_where(*[ctypes.byref(x) for x in v])
+    return {"code": int(code), "block": v[0].value, "thread": v[1].value, "tile": v[2].value,
+            "kblock": v[3].value}
 
 
 def mlp_tp_status_string(status: int) -> str:

@@ -23,7 +23,7 @@ struct GemmArgs {
 };
 
 // Defined in umma_gemm.cuh; explicitly instantiated once per flavour (gemm_*.cu).
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
 
 }  // namespace mlp

@@ -2,6 +2,7 @@
 #include "umma_gemm.cuh"
 
 namespace mlp {
-template cudaError_t launch_umma_gemm<128, false, true, EPI_BIAS_GELU>(const GemmArgs&, int, cudaStream_t);
-template cudaError_t launch_umma_gemm<256, false, true, EPI_BIAS_GELU>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<128, false, true, EPI_BIAS_GELU, 1>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, false, true, EPI_BIAS_GELU, 1>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, false, true, EPI_BIAS_GELU, 2>(const GemmArgs&, int, cudaStream_t);
 }  // namespace mlp

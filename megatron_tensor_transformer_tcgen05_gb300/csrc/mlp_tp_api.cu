@@ -16,8 +16,10 @@
 
 namespace mlp {
 
-// Device status word: kernels record the first bounded-wait failure here.
-__device__ int g_device_status;
+// Device status words: [0] = code of the first bounded wait that gave up (0 = none);
+// [1..4] = where: block index, thread index, tile, k block (or stage) of that wait.
+constexpr int kStatusWords = 8;
+__device__ int g_device_status[kStatusWords];
 
 // Limit for every bounded wait inside the GEMMs: one wait never lasts longer than one
 // tile's main loop (well under a millisecond), so two seconds only trips on a real stall.
@@ -33,7 +35,7 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 static DeviceInfo g_dev[kMaxDevices];
 static std::mutex g_dev_mu;
-static int g_last_code = 0;
+static int g_last_status[kStatusWords] = {0};
 
 static mlp_status device_info(DeviceInfo** out)
 {
@@ -51,7 +53,7 @@ static mlp_status device_info(DeviceInfo** out)
         d.num_sms = sms;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MLP_ECUDA;
-        d.status = static_cast<int*>(p);
+        d.status = static_cast<int*>(p);  // the first of kStatusWords words
         d.ready = true;
     }
     if (!d.supported) return MLP_EUNSUPPORTED;
@@ -110,14 +112,14 @@ static bool map_store(CUtensorMap* m, const void* p, uint64_t cols, uint64_t row
     return make_map(m, p, cols, rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-static int grid_for(int M, int N, int BN, int num_sms)
-{
-    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + BN - 1) / BN);
-    return static_cast<int>(tiles < num_sms ? tiles : num_sms);
-}
-
 // Tile width along N: 256 when the N extent splits into whole 256-wide tiles, else 128.
 static int tile_n(int n) { return (n % 256 == 0) ? 256 : 128; }
+
+// CTA pairs (256-row tiles, cta_group::2) for 256-wide tiles over more than 128 rows.
+static bool use_pairs(int M, int BN) { return BN == 256 && M > 128; }
+
+// Rows of a K-major B operand one CTA loads per stage: half the tile width for a pair.
+static uint32_t kmajor_b_box(int M, int BN) { return use_pairs(M, BN) ? BN / 2 : BN; }
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
@@ -126,10 +128,18 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
     // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
     // B block; otherwise sweep N fastest so they share one A block.
     g.n_fastest = g.M > g.N ? 1 : 0;
-    const int grid = grid_for(g.M, g.N, BN, num_sms);
+    const long long tiles_n = (g.N + BN - 1) / BN;
+    if (use_pairs(g.M, BN)) {
+        // CTA pairs: 256 x 256 tiles, one pair per two SMs.
+        const long long tiles = ((g.M + 255) / 256) * tiles_n;
+        const int pairs = static_cast<int>(tiles < num_sms / 2 ? tiles : num_sms / 2);
+        return launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s);
+    }
+    const long long tiles = ((g.M + 127) / 128) * tiles_n;
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     if (grid <= 0) return cudaSuccess;
-    return BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI>(g, grid, s)
-                     : launch_umma_gemm<128, A_MN, B_MN, EPI>(g, grid, s);
+    return BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, grid, s)
+                     : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, grid, s);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -323,7 +333,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
 
     // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h.
     GemmArgs g3{};
-    if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, bn_f) ||
+    if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, kmajor_b_box(T, bn_f)) ||
         !map_store(&g3.tmD0, dH, f, T))
         return MLP_ECUDA;
     g3.tmD1 = g3.tmD0;
@@ -337,7 +347,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
 
     // GEMM 4: dX = sum over shards of dH_i*A_i^T; A [h,f] is K-major for N = h, K = f.
     GemmArgs g4{};
-    if (!map_kmajor(&g4.tmA, dH, f, T, 128) || !map_kmajor(&g4.tmB, A, f, h, bn_h) ||
+    if (!map_kmajor(&g4.tmA, dH, f, T, 128) || !map_kmajor(&g4.tmB, A, f, h, kmajor_b_box(T, bn_h)) ||
         !map_store(&g4.tmD0, dX, h, T))
         return MLP_ECUDA;
     g4.tmD1 = g4.tmD0;
@@ -390,19 +400,28 @@ mlp_status mlp_tp_query_device_status(void* cuda_stream)
     mlp_status st = device_info(&dev);
     if (st != MLP_OK) return st;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return MLP_ECUDA;
-    int v = 0;
-    if (cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MLP_ECUDA;
-    if (v != 0) {
-        g_last_code = v;
-        const int zero = 0;
-        if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    int v[kStatusWords] = {0};
+    if (cudaMemcpy(v, dev->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MLP_ECUDA;
+    if (v[0] != 0) {
+        for (int i = 0; i < kStatusWords; ++i) g_last_status[i] = v[i];
+        const int zero[kStatusWords] = {0};
+        if (cudaMemcpy(dev->status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return MLP_ECUDA;
         return MLP_ETIMEOUT;
     }
     return MLP_OK;
 }
 
-int mlp_tp_last_device_code(void) { return g_last_code; }
+int mlp_tp_last_device_code(void) { return g_last_status[0]; }
+
+int mlp_tp_last_device_where(int* block, int* thread, int* tile, int* kblock)
+{
+    if (block) *block = g_last_status[1];
+    if (thread) *thread = g_last_status[2];
+    if (tile) *tile = g_last_status[3];
+    if (kblock) *kblock = g_last_status[4];
+    return g_last_status[0];
+}
 
 mlp_status mlp_tp_timing_enable(int on)
 {

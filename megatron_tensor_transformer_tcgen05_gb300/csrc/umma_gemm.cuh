@@ -32,13 +32,19 @@
 
 namespace mlp {
 
-template <int BN_, bool A_MN_, bool B_MN_, int EPI_>
+template <int BN_, bool A_MN_, bool B_MN_, int EPI_, int CG_>
 struct GemmCfg {
-    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = 4, UMMA_K = 16;
+    // CG = 1: one CTA computes a 128 x BN tile. CG = 2: a CTA pair (cluster of 2) computes a
+    // 256 x BN tile with cta_group::2 MMAs; each CTA holds 128 rows of A, BN/2 rows of B and
+    // its 128 x BN half of the accumulator.
+    static constexpr int CG = CG_;
+    static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
+    static constexpr int BN_CTA = BN / CG;  // rows of the B operand one CTA loads
+    static constexpr int STAGES = (CG == 2) ? 6 : 4;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
     static constexpr int EPI = EPI_;
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NOUT = (EPI == EPI_BIAS_GELU) ? 2 : 1;
     static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
@@ -48,8 +54,9 @@ struct GemmCfg {
     static constexpr uint32_t BAR_BYTES = 8 * NUM_BARS + 16;
     static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int THREADS = 192;
-    static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, BN, A_MN, B_MN);
     static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256-wide tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -124,22 +131,22 @@ __device__ __forceinline__ void stage_row_sw64(uint32_t buf, int lane, const uin
 // Output tile `tile` -> its first row and column. Consecutive tiles run at the same time on
 // neighbouring SMs, so the index that varies fastest decides which operand they share
 // through L2: M-fastest tiles share one B block and stream A, N-fastest share one A block.
-__device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, int n_fastest, int BN,
-                                            int& m0, int& n0)
+__device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, int n_fastest, int TM,
+                                            int BN, int& m0, int& n0)
 {
     if (n_fastest) {
-        m0 = (tile / tiles_n) * 128;
+        m0 = (tile / tiles_n) * TM;
         n0 = (tile % tiles_n) * BN;
     } else {
-        m0 = (tile % tiles_m) * 128;
+        m0 = (tile % tiles_m) * TM;
         n0 = (tile / tiles_m) * BN;
     }
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
 {
-    using C = GemmCfg<BN, A_MN, B_MN, EPI>;
+    using C = GemmCfg<BN, A_MN, B_MN, EPI, CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -156,8 +163,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (s_slot + 4u - base));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Pair mode: rank 0 (the even CTA) issues every MMA; rank r owns rows [128r, 128r+128)
+    // of each 256-row tile and B rows [r*BN/2, (r+1)*BN/2) of each stage.
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int unit = (CG == 2) ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+    const int num_units = (CG == 2) ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
     const int M = args.M, N = args.N, K = args.K;
-    const int tiles_m = (M + C::BM - 1) / C::BM;
+    const int TM = C::BM * CG;  // rows per tile
+    const int tiles_m = (M + TM - 1) / TM;
     const int tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (K + C::BK - 1) / C::BK;
@@ -170,7 +183,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(b_accf + 8u * a, 1);
-            mbar_init(b_acce + 8u * a, 4);  // one arrive per epilogue warp
+            mbar_init(b_acce + 8u * a, 4 * CG);  // one arrive per epilogue warp of the pair
         }
         mbar_init(b_drain, 1);
         *abort_flag = 0;
@@ -180,12 +193,21 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         tma_prefetch_desc(&args.tmD0);
         if (C::NOUT == 2) tma_prefetch_desc(&args.tmD1);
     }
+    if (CG == 2) cluster_sync();  // the peer CTA is running before the collective allocation
     if (warp == 1) {
-        tmem_alloc(s_slot, C::TMEM_COLS);
-        tmem_relinquish();
+        if (CG == 2) {
+            tmem_alloc_pair(s_slot, C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(s_slot, C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (CG == 2)
+        cluster_sync();  // both CTAs' barriers and TMEM exist before either signals the other
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -194,12 +216,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0, par = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 int m0, n0;
-                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, BN, m0, n0);
+                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, TM, BN, m0, n0);
+                const int m_cta = m0 + C::BM * static_cast<int>(rank);
+                const int n_cta = n0 + C::BN_CTA * static_cast<int>(rank);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_bounded(b_empty + 8u * stage, phase ^ 1u, abort_flag, args.status,
-                                           limit, DEV_TIMEOUT_PRODUCER)) {
+                                           limit, DEV_TIMEOUT_PRODUCER, tile, kb)) {
                         ok = false;
                         break;
                     }
@@ -207,19 +231,39 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     const uint32_t sb = sa + C::A_BYTES;
                     const uint32_t fb = b_full + 8u * stage;
                     const int k0 = kb * C::BK;
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    if (A_MN) {
-                        tma_load_2d(sa, &args.tmA, m0, k0, fb);
-                        tma_load_2d(sa + 8192u, &args.tmA, m0 + 64, k0, fb);
-                    } else {
-                        tma_load_2d(sa, &args.tmA, k0, m0, fb);
-                    }
-                    if (B_MN) {
+                    if (CG == 1) {
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        if (A_MN) {
+                            tma_load_2d(sa, &args.tmA, m_cta, k0, fb);
+                            tma_load_2d(sa + 8192u, &args.tmA, m_cta + 64, k0, fb);
+                        } else {
+                            tma_load_2d(sa, &args.tmA, k0, m_cta, fb);
+                        }
+                        if (B_MN) {
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tma_load_2d(sb + 8192u * i, &args.tmB, n0 + 64 * i, k0, fb);
+                            for (int i = 0; i < C::BN_CTA / 64; ++i)
+                                tma_load_2d(sb + 8192u * i, &args.tmB, n_cta + 64 * i, k0, fb);
+                        } else {
+                            tma_load_2d(sb, &args.tmB, k0, n_cta, fb);
+                        }
                     } else {
-                        tma_load_2d(sb, &args.tmB, k0, n0, fb);
+                        // Both CTAs' bytes complete on the even CTA's barrier, which the even
+                        // CTA alone arms with the pair's total.
+                        const uint32_t fb0 = mapa_shared(fb, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+                        if (A_MN) {
+                            tma_load_2d_pair(sa, &args.tmA, m_cta, k0, fb0);
+                            tma_load_2d_pair(sa + 8192u, &args.tmA, m_cta + 64, k0, fb0);
+                        } else {
+                            tma_load_2d_pair(sa, &args.tmA, k0, m_cta, fb0);
+                        }
+                        if (B_MN) {
+#pragma unroll
+                            for (int i = 0; i < C::BN_CTA / 64; ++i)
+                                tma_load_2d_pair(sb + 8192u * i, &args.tmB, n_cta + 64 * i, k0, fb0);
+                        } else {
+                            tma_load_2d_pair(sb, &args.tmB, k0, n_cta, fb0);
+                        }
                     }
                     issued |= 1u << stage;
                     par = (par & ~(1u << stage)) | (phase << stage);
@@ -230,22 +274,26 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 }
             }
             if (!ok) {
-                // Let every copy this thread started land before the CTA may exit.
-                volatile int never = 0;
-                for (int s = 0; s < C::STAGES; ++s)
-                    if (issued & (1u << s))
-                        mbar_wait_bounded(b_full + 8u * s, (par >> s) & 1u, &never, args.status,
-                                          kDrainLimitNs, DEV_TIMEOUT_DRAIN);
+                // Let every copy this CTA started land before the CTA may exit.
+                if (rank == 0) {
+                    volatile int never = 0;
+                    for (int s = 0; s < C::STAGES; ++s)
+                        if (issued & (1u << s))
+                            mbar_wait_bounded(b_full + 8u * s, (par >> s) & 1u, &never, args.status,
+                                              kDrainLimitNs, DEV_TIMEOUT_DRAIN);
+                } else if (issued) {
+                    spin_ns(2000000ull);  // its barrier lives in the even CTA: give them 2 ms
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true, any = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 if (!mbar_wait_bounded(b_acce + 8u * acc, acc_phase ^ 1u, abort_flag, args.status,
-                                       limit, DEV_TIMEOUT_MMA_ACC)) {
+                                       limit, DEV_TIMEOUT_MMA_ACC, tile, -1)) {
                     ok = false;
                     break;
                 }
@@ -253,7 +301,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_bounded(b_full + 8u * stage, phase, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_FULL)) {
+                                           DEV_TIMEOUT_MMA_FULL, tile, kb)) {
                         ok = false;
                         break;
                     }
@@ -268,44 +316,60 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                                                  : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
                         const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
                                                  : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-                        umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                        if (CG == 2)
+                            umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
                     any = true;
-                    umma_commit(b_empty + 8u * stage);  // stage is free once these MMAs finish
+                    // the stage is free, in both CTAs, once these MMAs finish
+                    if (CG == 2)
+                        umma_commit_pair_mc(b_empty + 8u * stage, 0x3);
+                    else
+                        umma_commit(b_empty + 8u * stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(b_accf + 8u * acc);  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue warps of both CTAs
+                if (CG == 2)
+                    umma_commit_pair_mc(b_accf + 8u * acc, 0x3);
+                else
+                    umma_commit(b_accf + 8u * acc);
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (!ok && any) {
                 // Let the MMAs already issued finish before TMEM is released.
                 volatile int never = 0;
-                umma_commit(b_drain);
+                if (CG == 2)
+                    umma_commit_pair(b_drain);
+                else
+                    umma_commit(b_drain);
                 mbar_wait_bounded(b_drain, 0, &never, args.status, kDrainLimitNs, DEV_TIMEOUT_DRAIN);
             }
         }
     } else {
         // ------------------------------ epilogue ----------------------------------
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the ones this warp may read
+        // accumulator release goes to the even CTA, which issues the MMAs
+        const uint32_t acce0 = (CG == 2) ? mapa_shared(b_acce, 0) : b_acce;
         uint32_t acc = 0, acc_phase = 0, sel = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = unit; tile < num_tiles; tile += num_units) {
             // One lane waits; the warp follows its verdict so the .sync.aligned TMEM loads
             // below always run with all 32 lanes.
             int ready = 0;
             if (lane == 0)
                 ready = mbar_wait_bounded(b_accf + 8u * acc, acc_phase, abort_flag, args.status, limit,
-                                          DEV_TIMEOUT_EPILOGUE);
+                                          DEV_TIMEOUT_EPILOGUE, tile, -1);
             ready = __shfl_sync(0xffffffffu, ready, 0);
             if (!ready) break;
             tc_fence_after();
             int m0, n0;
-            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, BN, m0, n0);
-            const int row_blk = m0 + 32 * q;
+            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, TM, BN, m0, n0);
+            const int row_blk = m0 + C::BM * static_cast<int>(rank) + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
@@ -331,7 +395,12 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 if (c == BN / 32 - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(b_acce + 8u * acc);  // accumulator may be reused
+                    if (lane == 0) {  // accumulator may be reused
+                        if (CG == 2)
+                            mbar_arrive_cluster(acce0 + 8u * acc);
+                        else
+                            mbar_arrive(b_acce + 8u * acc);
+                    }
                 }
                 if (!active || row_blk >= M) continue;
 
@@ -395,21 +464,43 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (CG == 2)
+        cluster_sync();  // the even CTA's MMAs touch both CTAs' TMEM and shared memory
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if (CG == 2)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 // Host-side launcher, instantiated once per GEMM flavour in its own translation unit.
-template <int BN, bool A_MN, bool B_MN, int EPI>
+// `grid` counts CTAs (a multiple of CG).
+template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream)
 {
-    using C = GemmCfg<BN, A_MN, B_MN, EPI>;
-    auto kern = umma_gemm_kernel<BN, A_MN, B_MN, EPI>;
+    using C = GemmCfg<BN, A_MN, B_MN, EPI, CG>;
+    auto kern = umma_gemm_kernel<BN, A_MN, B_MN, EPI, CG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(args);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -33,7 +33,8 @@ def _run(inp_cpu: dict, t: int):
     f = inp_cpu["A"].shape[1]
     buf = block.empty_buffers(T, h, f, t)
     block.step(dev, buf, t)
-    assert _lib.mlp_tp_query_device_status() == 0
+    st = _lib.mlp_tp_query_device_status()
+    assert st == 0, f"device status {st}: {_lib.mlp_tp_last_device_where()}"
     return dev, buf
 
 
