@@ -15,6 +15,7 @@ struct GemmArgs {
     CUtensorMap tmD1;   // second output (G of EPI_BIAS_GELU), same box
     int M, N, K;
     int n_fastest;               // tile order: 0 = M index fastest, 1 = N index fastest
+    int raster_group;            // tiles of the fast index per group (<= 0: all of them)
     const __nv_bfloat16* bias;   // [N] for EPI_BIAS / EPI_BIAS_GELU
     const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU
     long long ld_aux;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -128,6 +129,10 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
     // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
     // B block; otherwise sweep N fastest so they share one A block.
     g.n_fastest = g.M > g.N ? 1 : 0;
+    // Group ~sqrt(units) tiles of the fast dimension: a wave then touches the fewest
+    // distinct operand blocks (DRAM traffic at 18B: 3.8-5.3 GB -> 2.5-2.9 GB per GEMM).
+    const int units = use_pairs(g.M, BN) ? num_sms / 2 : num_sms;
+    g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(units > 1 ? units : 1))));
     const long long tiles_n = (g.N + BN - 1) / BN;
     if (use_pairs(g.M, BN)) {
         // CTA pairs: 256 x 256 tiles, one pair per two SMs.

@@ -67,6 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Same test, but a thread whose phase is not complete may sleep until it completes (or
+// for up to `hint_ns`) instead of returning at once: waiting costs no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kWaitSleepHintNs = 10000000u;  // wakes on completion; the hint only caps the nap
+
 // Wait for the phase with the given parity to complete. Gives up (returns false) when
 // *abort is set by another role, or after limit_ns; on a timeout it records `code` in
 // status[0] (first error wins; then status[1..4] = block, thread, where_a, where_b) and
@@ -79,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
         if ((it & 15u) == 0u) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {

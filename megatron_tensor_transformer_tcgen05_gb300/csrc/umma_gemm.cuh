@@ -128,18 +128,30 @@ __device__ __forceinline__ void stage_row_sw64(uint32_t buf, int lane, const uin
         sts_v4(row + ((j ^ x) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
 }
 
-// Output tile `tile` -> its first row and column. Consecutive tiles run at the same time on
-// neighbouring SMs, so the index that varies fastest decides which operand they share
-// through L2: M-fastest tiles share one B block and stream A, N-fastest share one A block.
-__device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, int n_fastest, int TM,
+// Output tile `tile` -> its first row and column. Tiles that run at the same time (about
+// one per unit, consecutive indices) share operand blocks through L2 while their k loops
+// run in step; with large K nothing survives in L2 from one wave to the next, so a wave
+// reads every distinct A and B block it touches from DRAM. Tiles are therefore ordered
+// in groups of `group` consecutive indices along the fast dimension (M, or N when
+// n_fastest), sweeping the other dimension within a group: a wave covers about
+// group x (units / group) tiles and reads group + units / group blocks instead of
+// (all of the fast dimension) + (units / that).
+__device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, int n_fastest, int group, int TM,
                                             int BN, int& m0, int& n0)
 {
+    const int fast_n = n_fastest ? tiles_n : tiles_m;  // extent of the grouped index
+    const int slow_n = n_fastest ? tiles_m : tiles_n;
+    const int gsz = (group > 0 && group < fast_n) ? group : fast_n;
+    const int per_group = gsz * slow_n;
+    const int g = tile / per_group, r = tile % per_group;
+    const int glen = min(gsz, fast_n - g * gsz);
+    const int fast = g * gsz + r % glen, slow = r / glen;
     if (n_fastest) {
-        m0 = (tile / tiles_n) * TM;
-        n0 = (tile % tiles_n) * BN;
+        m0 = slow * TM;
+        n0 = fast * BN;
     } else {
-        m0 = (tile % tiles_m) * TM;
-        n0 = (tile / tiles_m) * BN;
+        m0 = fast * TM;
+        n0 = slow * BN;
     }
 }
 
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             bool ok = true;
             for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 int m0, n0;
-                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, TM, BN, m0, n0);
+                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, BN, m0, n0);
                 const int m_cta = m0 + C::BM * static_cast<int>(rank);
                 const int n_cta = n0 + C::BN_CTA * static_cast<int>(rank);
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             if (!ready) break;
             tc_fence_after();
             int m0, n0;
-            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, TM, BN, m0, n0);
+            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, BN, m0, n0);
             const int row_blk = m0 + C::BM * static_cast<int>(rank) + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
