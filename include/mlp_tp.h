@@ -74,7 +74,8 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
  *   dH = (dY*B^T) (.) GELU'(H)        per shard, GELU' in the GEMM epilogue
  *   dX = dH*A^T = sum_i dH_i A_i^T    shard sum in one accumulator
  *   dA = X^T*dH,  dB = G^T*dY         local weight gradients
- *   da = colsum(dH) (fp32),  db = colsum(dY) (fp32)
+ *   da = colsum(dH) (fp32; the dH GEMM sums its fp32 dH over 32-row blocks in the
+ *        epilogue),  db = colsum(dY) (fp32)
  * `workspace` (device, >= mlp_tp_workspace_bytes(T,h,f,t) bytes, 256-byte aligned) holds
  * dH and the reduction partials; its contents on entry do not matter. On return its first
  * T*f*2 bytes hold dH = dL/dH (row-major bf16 [T,f]). Six launches. */
@@ -142,7 +143,7 @@ enum {
     MLP_K_BWD_DX = 3,        /* dX = dH*A^T */
     MLP_K_BWD_DA = 4,        /* dA = X^T*dH */
     MLP_K_BWD_DB = 5,        /* dB = G^T*dY */
-    MLP_K_COLSUM_PARTIAL = 6,/* da, db partial column sums */
+    MLP_K_COLSUM_PARTIAL = 6,/* db partial column sums (da's come from the dH GEMM) */
     MLP_K_COLSUM_FINAL = 7,  /* da, db final sums */
     MLP_NUM_KERNELS = 8
 };

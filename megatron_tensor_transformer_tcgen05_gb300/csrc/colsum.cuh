@@ -1,4 +1,7 @@
 // colsum.cuh -- bias-gradient column reductions da[j] = sum_r dH[r,j], db[j] = sum_r dY[r,j].
+// In the backward pass the dH GEMM's epilogue already sums dH over each 32-row block, so
+// only dY goes through the partial pass here; the entry point without a workspace reduces
+// both matrices with these kernels.
 //
 // Memory-bound. Each warp reads 4 rows x 64 columns per step with 16-byte vector loads
 // (lane = 8 columns of one row; 8 lanes cover one 128-byte row segment), keeps 8 fp32
@@ -103,6 +106,26 @@ __global__ void colsum_finalize_kernel(const float* __restrict__ partial, int ns
         out1[c] = t;
     else
         out2[c - cols1] = t;
+}
+
+// da[c] = sum over 32-row blocks rb of rows[rb][c] (written by the dH GEMM's epilogue);
+// db[c] = sum over slices s of partial[s][c] (from colsum_partial_kernel over dY alone).
+// Both sums run in index order, so the results are bitwise reproducible.
+__global__ void bias_grad_finalize_kernel(const float* __restrict__ rows, int nrb, int f,
+                                          const float* __restrict__ partial, int nsplit, int h,
+                                          float* __restrict__ da, float* __restrict__ db)
+{
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c < f) {
+        float t = 0.f;
+        for (int rb = 0; rb < nrb; ++rb) t += rows[static_cast<long long>(rb) * f + c];
+        da[c] = t;
+    } else if (c < f + h) {
+        const int j = c - f;
+        float t = 0.f;
+        for (int s = 0; s < nsplit; ++s) t += partial[static_cast<long long>(s) * h + j];
+        db[j] = t;
+    }
 }
 
 }  // namespace mlp

@@ -18,6 +18,8 @@ struct GemmArgs {
     int raster_group;            // tiles of the fast index per group (<= 0: all of them)
     const __nv_bfloat16* bias;   // [N] for EPI_BIAS / EPI_BIAS_GELU
     const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU
+    float* colsum_rows;          // EPI_DGELU, optional: per-32-row column sums of D (fp32),
+                                 // [ceil(M/32), N] row-major; NULL = not wanted
     long long ld_aux;
     int* status;                 // device status word (first error code wins)
     unsigned long long timeout_ns;

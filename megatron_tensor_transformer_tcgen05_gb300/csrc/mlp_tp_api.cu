@@ -240,12 +240,16 @@ const char* mlp_tp_status_string(mlp_status s)
     return "unknown mlp_status";
 }
 
+// Backward workspace: dH [T,f] bf16 | dH column sums per 32-row block [ceil(T/32), f] fp32 |
+// dY column sums per row slice [slices, h] fp32 (each region 256-byte aligned).
+static size_t ws_dh_bytes(int T, int f) { return round256(static_cast<size_t>(T) * f * 2); }
+static size_t ws_rows_bytes(int T, int f) { return round256(static_cast<size_t>((T + 31) / 32) * f * 4); }
+static size_t ws_dy_bytes(int T, int h) { return round256(static_cast<size_t>(colsum_splits(T)) * h * 4); }
+
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t)
 {
     if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    const size_t dh = round256(static_cast<size_t>(T) * f * 2);
-    const size_t part = round256(static_cast<size_t>(colsum_splits(T)) * (static_cast<size_t>(f) + h) * 4);
-    return dh + part;
+    return ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
 }
 
 int mlp_tp_launches_per_call(int backward, int T)
@@ -332,7 +336,8 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
-    float* partial = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(T) * f * 2));
+    float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f));
+    float* dy_part = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + ws_rows_bytes(T, f));
     const int nsplit = colsum_splits(T);
     CallTimer timer(s);
 
@@ -345,6 +350,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     g3.M = T; g3.N = f; g3.K = h;
     g3.aux = reinterpret_cast<const __nv_bfloat16*>(H);
     g3.ld_aux = f;
+    g3.colsum_rows = dh_rows;  // da's per-32-row partial sums come out of this epilogue
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
     if (gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
@@ -386,14 +392,15 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DB);
 
-    // Bias gradients: da = colsum(dH), db = colsum(dY), two passes, fixed order.
-    const int strips = (f + kColsumStrip - 1) / kColsumStrip + (h + kColsumStrip - 1) / kColsumStrip;
-    colsum_partial_kernel<<<dim3(strips, nsplit), kColsumThreads, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(dH), f, reinterpret_cast<const __nv_bfloat16*>(dY), h,
-        T, nsplit, partial);
+    // Bias gradients: db's partial column sums over row slices of dY (da's came out of the
+    // dH GEMM), then one pass adding both sets of partials in a fixed order.
+    const int strips_h = (h + kColsumStrip - 1) / kColsumStrip;
+    colsum_partial_kernel<<<dim3(strips_h, nsplit), kColsumThreads, 0, s>>>(
+        nullptr, 0, reinterpret_cast<const __nv_bfloat16*>(dY), h, T, nsplit, dy_part);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_COLSUM_PARTIAL);
-    colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
+    bias_grad_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(dh_rows, (T + 31) / 32, f, dy_part, nsplit, h,
+                                                                  da, db);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_COLSUM_FINAL);
     return MLP_OK;
@@ -472,7 +479,7 @@ const char* mlp_tp_kernel_name(int kernel)
     static const char* names[MLP_NUM_KERNELS] = {
         "gemm_fwd_up (H=XA+a, G=GELU(H))", "gemm_fwd_down (Y=GB+b)", "gemm_bwd_dh (dH=dY B^T * GELU'(H))",
         "gemm_bwd_dx (dX=dH A^T)",          "gemm_bwd_da (dA=X^T dH)", "gemm_bwd_db (dB=G^T dY)",
-        "colsum_partial (da, db)",          "colsum_finalize (da, db)"};
+        "colsum_partial (db)",              "bias_grad_finalize (da, db)"};
     return (kernel >= 0 && kernel < MLP_NUM_KERNELS) ? names[kernel] : "unknown";
 }
 

@@ -18,7 +18,8 @@
 // Epilogues (the step of the MLP block each one implements):
 //   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H)            -> stores H and G
 //   EPI_BIAS       Y = acc + b[n]                          -> stores Y
-//   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH
+//   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH (and, optionally,
+//                  its column sums over each 32-row block in fp32, for the bias gradient)
 //   EPI_PLAIN      D = acc                                 -> stores D
 // GELU is the tanh form 0.5 x (1 + tanh u), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated
 // through the identity 1 + tanh u = 2 / (1 + exp(-2u)), which stays accurate where
@@ -114,6 +115,24 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+// Column sums over the 32 lanes of a warp: lane l holds v[0..31] (its row, 32 columns);
+// afterwards v[0] of lane l is the sum over all lanes of column l. Five halving stages,
+// 31 shuffles: at stage s each lane keeps the half of its columns selected by bit s of
+// its lane index and adds the partner's copy of that half.
+__device__ __forceinline__ void warp_column_sums(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int j = 0; j < s; ++j) {
+            const float send = upper ? v[j] : v[j + s];
+            const float keep = upper ? v[j + s] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
 }
 
 // Write one thread's 32 bf16 (16 packed words) as row `lane` of a 32x32 box laid out the
@@ -446,6 +465,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(hv[j]);
+                    if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
+                        float cs[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) cs[j] = v[j];
+                        warp_column_sums(cs, lane);
+                        if (nc + lane < N)
+                            args.colsum_rows[static_cast<size_t>(row_blk >> 5) * N + nc + lane] = cs[0];
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
