@@ -57,6 +57,14 @@ def _load():
             lib.oracle_mlp_sampled_bf16.restype = i32
             lib.oracle_mlp_sampled_bf16.argtypes = ([i64, i64, i64, i32] + [dp] * 6 +
                                                     [i64, dp, i64, dp] + [dp] * 6)
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_philox4x32_10.argtypes = [dp, dp, dp]
+            lib.oracle_dropout_keep.restype = i32
+            lib.oracle_dropout_keep.argtypes = [i64, i64, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64, dp]
+            lib.oracle_residual_dropout.restype = i32
+            lib.oracle_residual_dropout.argtypes = [i64, i64, ctypes.c_double, dp, dp, dp, dp]
+            lib.oracle_dropout_backward.restype = i32
+            lib.oracle_dropout_backward.argtypes = [i64, i64, ctypes.c_double, dp, dp, dp]
             _lib = lib
     return _lib
 
@@ -178,3 +186,62 @@ def sampled_bf16(inp: dict, rows, cols, act: str = "gelu_tanh") -> dict:
     assert rc == 0, rc
     return {"Y_rows": Yr, "dX_rows": dXr, "dA_cols": dAc.T.copy(), "dB_rows": dBc, "da": dac,
             "db": db}
+
+
+# ---- bias + dropout + residual add on the block output ----------------------------------
+
+def philox4x32_10(counter, key) -> tuple:
+    """Philox4x32-10 of one 128-bit counter (4 uint32) under a 64-bit key (2 uint32)."""
+    lib = _load()
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(_p(c), _p(k), _p(out))
+    return tuple(int(v) for v in out)
+
+
+def dropout_keep(T: int, h: int, p: float, seed: int, offset: int = 0) -> np.ndarray:
+    """Keep mask (uint8 0/1, [T,h]) of dropout with probability p."""
+    lib = _load()
+    keep = np.empty((T, h), dtype=np.uint8)
+    rc = lib.oracle_dropout_keep(T, h, float(p), int(seed), int(offset), _p(keep))
+    if rc != 0:
+        raise ValueError(f"bad dropout arguments p={p}")
+    return keep
+
+
+def residual_dropout(Y, R, keep, p: float) -> np.ndarray:
+    """Z = R + keep * Y / (1 - p)."""
+    lib = _load()
+    Y, R = _f64(Y), _f64(R)
+    keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    T, h = Y.shape
+    Z = np.empty((T, h))
+    rc = lib.oracle_residual_dropout(T, h, float(p), _p(Y), _p(R), _p(keep), _p(Z))
+    assert rc == 0, rc
+    return Z
+
+
+def dropout_backward(dZ, keep, p: float) -> np.ndarray:
+    """dL/dY = dL/dZ * keep / (1 - p)."""
+    lib = _load()
+    dZ = _f64(dZ)
+    keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    T, h = dZ.shape
+    dY = np.empty((T, h))
+    rc = lib.oracle_dropout_backward(T, h, float(p), _p(dZ), _p(keep), _p(dY))
+    assert rc == 0, rc
+    return dY
+
+
+def fwd_bwd_residual_dropout(inp: dict, R, dZ, p: float, seed: int, offset: int = 0,
+                             act: str = "gelu_tanh") -> dict:
+    """The block followed by bias + dropout + residual add: Z, and every gradient given dZ."""
+    T, h = _f64(inp["X"]).shape
+    keep = dropout_keep(T, h, p, seed, offset)
+    H, G, Y = forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], act)
+    Z = residual_dropout(Y, R, keep, p)
+    dY = dropout_backward(dZ, keep, p)
+    out = backward(inp["X"], inp["A"], inp["B"], H, G, dY, act)
+    out.update(H=H, G=G, Y=Y, Z=Z, keep=keep, dY=dY, dR=_f64(dZ))
+    return out

@@ -399,3 +399,72 @@ int oracle_mlp_sampled_bf16(int64_t T, int64_t h, int64_t f, int act,
     }
     return 0;
 }
+
+/* ---- bias + dropout + residual add on the block output ------------------------------ */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC 2011): ten rounds of the 4x32 Philox S-box on a 128-bit counter, keyed by a 64-bit key
+ * that is bumped by the Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0; /* multiplier of the first pair */
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2; /* multiplier of the second pair */
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Dropout keep mask of a [T,h] tensor: element e = r*h + c draws word (e % 4) of Philox on
+ * counter (lo32(e/4), hi32(e/4), lo32(offset), hi32(offset)) with key (lo32(seed),
+ * hi32(seed)); its top 24 bits u24 keep the element when u24 >= floor(p * 2^24). */
+int oracle_dropout_keep(int64_t T, int64_t h, double p, uint64_t seed, uint64_t offset, uint8_t *keep)
+{
+    if (T < 0 || h < 1 || !(p >= 0.0 && p < 1.0)) return 1;
+    const uint32_t p24 = (uint32_t)floor(p * 16777216.0);
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    const int64_t n = T * h;
+#pragma omp parallel for schedule(static)
+    for (int64_t q = 0; q < (n + 3) / 4; ++q) {
+        uint32_t ctr[4] = {(uint32_t)q, (uint32_t)((uint64_t)q >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)};
+        uint32_t out[4];
+        oracle_philox4x32_10(ctr, key, out);
+        for (int w = 0; w < 4; ++w) {
+            int64_t e = 4 * q + w;
+            if (e < n) keep[e] = (uint8_t)((out[w] >> 8) >= p24);
+        }
+    }
+    return 0;
+}
+
+/* The fused output step of "Efficient Large-Scale Language Model Training ... Megatron-LM"
+ * (section 3, "Fused element-wise kernels": bias + dropout + residual add), applied to the
+ * block output of Figure 5a (Z = Dropout(Y B)) with the residual stream R:
+ *   Z = R + keep (.) (G B + b) / (1 - p)        with Y = G B + b from oracle_mlp_forward.
+ * Backward: dL/dY = dL/dZ (.) keep / (1 - p), dL/dR = dL/dZ. */
+int oracle_residual_dropout(int64_t T, int64_t h, double p, const double *Y, const double *R,
+                            const uint8_t *keep, double *Z)
+{
+    if (T < 0 || h < 1 || !(p >= 0.0 && p < 1.0)) return 1;
+    const double scale = 1.0 / (1.0 - p);
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < T * h; ++e) Z[e] = R[e] + (keep[e] ? Y[e] * scale : 0.0);
+    return 0;
+}
+
+int oracle_dropout_backward(int64_t T, int64_t h, double p, const double *dZ, const uint8_t *keep, double *dY)
+{
+    if (T < 0 || h < 1 || !(p >= 0.0 && p < 1.0)) return 1;
+    const double scale = 1.0 / (1.0 - p);
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < T * h; ++e) dY[e] = keep[e] ? dZ[e] * scale : 0.0;
+    return 0;
+}
