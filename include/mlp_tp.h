@@ -70,6 +70,28 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
                           const mlp_bf16* B, const mlp_bf16* b, int T, int h, int f, int t,
                           mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* cuda_stream);
 
+/* Forward pass followed by the block's fused output step ("Efficient Large-Scale Language
+ * Model Training on GPU Clusters Using Megatron-LM", section 3, "Fused element-wise
+ * kernels": bias + dropout + residual add, on the output of Figure 5a, Z = Dropout(Y B)):
+ *     Z = R + keep (.) (G*B + b) / (1 - p)
+ * R [T,h] is the residual stream (bf16). keep is drawn per element with Philox4x32-10
+ * (Salmon et al., SC 2011): element e = r*h + c uses word e % 4 of Philox on counter
+ * (lo32(e/4), hi32(e/4), lo32(offset), hi32(offset)) with key (lo32(seed), hi32(seed)) and
+ * is kept when that word's top 24 bits are >= floor(p * 2^24); 0 <= p < 1 (else
+ * MLP_EINVAL). H and G are written as by mlp_tp_forward; Y itself is not, Z takes its
+ * place (both in the epilogue of the second GEMM). Same launches as mlp_tp_forward. */
+mlp_status mlp_tp_forward_residual_dropout(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
+                                           const mlp_bf16* B, const mlp_bf16* b, const mlp_bf16* R,
+                                           int T, int h, int f, int t, double p,
+                                           unsigned long long seed, unsigned long long offset,
+                                           mlp_bf16* H, mlp_bf16* G, mlp_bf16* Z, void* cuda_stream);
+
+/* Backward of that output step: dY = dZ (.) keep / (1 - p) with the same (p, seed, offset),
+ * so the mask is regenerated, never stored. dL/dR is dZ itself. Feed dY to
+ * mlp_tp_backward. dZ, dY [T,h] bf16; h >= 8 and a multiple of 8. One launch. */
+mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, unsigned long long seed,
+                                   unsigned long long offset, mlp_bf16* dY, void* cuda_stream);
+
 /* Backward pass given dY = dL/dY ("Parallelism", "The backward pass"; chain rule):
  *   dH = (dY*B^T) (.) GELU'(H)        per shard, GELU' in the GEMM epilogue
  *   dX = dH*A^T = sum_i dH_i A_i^T    shard sum in one accumulator
@@ -145,7 +167,8 @@ enum {
     MLP_K_BWD_DB = 5,        /* dB = G^T*dY */
     MLP_K_COLSUM_PARTIAL = 6,/* db partial column sums (da's come from the dH GEMM) */
     MLP_K_COLSUM_FINAL = 7,  /* da, db final sums */
-    MLP_NUM_KERNELS = 8
+    MLP_K_DROPOUT_BWD = 8,   /* dY = dZ (.) keep / (1 - p) */
+    MLP_NUM_KERNELS = 9
 };
 mlp_status mlp_tp_timing_enable(int on);
 mlp_status mlp_tp_timing_collect(double* ms, int* counts);

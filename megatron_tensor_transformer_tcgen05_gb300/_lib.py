@@ -71,6 +71,11 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_timing_collect.argtypes = [vp, vp]
             L.mlp_tp_kernel_name.restype = ctypes.c_char_p
             L.mlp_tp_kernel_name.argtypes = [i32]
+            L.mlp_tp_forward_residual_dropout.restype = i32
+            L.mlp_tp_forward_residual_dropout.argtypes = ([vp] * 6 + [i32] * 4 + [ctypes.c_double, u64, u64] +
+                                                          [vp] * 3 + [vp])
+            L.mlp_tp_dropout_backward.restype = i32
+            L.mlp_tp_dropout_backward.argtypes = [vp, i32, i32, ctypes.c_double, u64, u64, vp, vp]
             L.mlp_tp_bias_grads_noalloc.restype = i32
             L.mlp_tp_bias_grads_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
             _lib = L
@@ -145,7 +150,7 @@ def mlp_tp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
            "mlp_tp_selftest_wait_timeout")
 
 
-MLP_NUM_KERNELS = 8
+MLP_NUM_KERNELS = 9
 
 
 def mlp_tp_timing_enable(on: bool) -> None:
@@ -168,3 +173,15 @@ def mlp_tp_bias_grads_noalloc(dH, dY, T: int, h: int, f: int, da, db, stream=Non
     scratch array holds the partial sums (see include/mlp_tp.h for its limit)."""
     _check(lib().mlp_tp_bias_grads_noalloc(_ptr(dH), _ptr(dY), T, h, f, _ptr(da), _ptr(db),
                                            _stream(stream)), "mlp_tp_bias_grads_noalloc")
+
+
+def mlp_tp_forward_residual_dropout(X, A, a, B, b, R, T: int, h: int, f: int, t: int, p: float, seed: int,
+                                    offset: int, H, G, Z, stream=None) -> None:
+    _check(lib().mlp_tp_forward_residual_dropout(_ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), _ptr(R), T, h,
+                                                 f, t, float(p), int(seed), int(offset), _ptr(H), _ptr(G),
+                                                 _ptr(Z), _stream(stream)), "mlp_tp_forward_residual_dropout")
+
+
+def mlp_tp_dropout_backward(dZ, T: int, h: int, p: float, seed: int, offset: int, dY, stream=None) -> None:
+    _check(lib().mlp_tp_dropout_backward(_ptr(dZ), T, h, float(p), int(seed), int(offset), _ptr(dY),
+                                         _stream(stream)), "mlp_tp_dropout_backward")

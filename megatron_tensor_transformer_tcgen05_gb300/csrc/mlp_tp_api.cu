@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "colsum.cuh"
+#include "dropout.cuh"
 #include "gemm_args.h"
 #include "mlp_tp.h"
 #include "sm103_ptx.cuh"
@@ -258,15 +259,21 @@ int mlp_tp_launches_per_call(int backward, int T)
     return backward ? 6 : 2;
 }
 
-mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
-                          const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* G,
-                          mlp_bf16* Y, void* cuda_stream)
+}  // extern "C"
+
+namespace mlp {
+
+// The forward pass; with `drop` set, GEMM 2's epilogue also applies dropout and adds the
+// residual R, writing Z instead of Y.
+static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
+                               const mlp_bf16* b, const mlp_bf16* R, const DropoutParams* drop, int T, int h,
+                               int f, int t, mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* cuda_stream)
 {
     mlp_status st = check_shape(T, h, f, t);
     if (st != MLP_OK) return st;
     // Token-indexed buffers may be NULL only when there are no tokens.
-    if (!A || !a || !B || !b || (T > 0 && (!X || !H || !G || !Y))) return MLP_EINVAL;
-    const void* ptrs[] = {X, A, a, B, b, H, G, Y};
+    if (!A || !a || !B || !b || (T > 0 && (!X || !H || !G || !Y || (drop && !R)))) return MLP_EINVAL;
+    const void* ptrs[] = {X, A, a, B, b, H, G, Y, R};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
     DeviceInfo* dev = nullptr;
@@ -289,7 +296,8 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
     if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_UP);
 
-    // GEMM 2: Y = sum over shards of G_i*B_i, + b. One accumulator over K = f.
+    // GEMM 2: Y = sum over shards of G_i*B_i, + b (then dropout and + R). One accumulator
+    // over K = f.
     GemmArgs g2{};
     if (!map_kmajor(&g2.tmA, G, f, T, 128) || !map_mnmajor(&g2.tmB, B, h, f) ||
         !map_store(&g2.tmD0, Y, h, T))
@@ -299,8 +307,76 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
     g2.bias = reinterpret_cast<const __nv_bfloat16*>(b);
     g2.status = dev->status;
     g2.timeout_ns = kWaitLimitNs;
-    if (gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    cudaError_t e;
+    if (drop) {
+        g2.aux = reinterpret_cast<const __nv_bfloat16*>(R);
+        g2.ld_aux = h;
+        g2.drop = *drop;
+        e = gemm<false, true, EPI_BIAS_DROPOUT_RES>(g2, bn_h, dev->num_sms, s);
+    } else {
+        e = gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s);
+    }
+    if (e != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_DOWN);
+    return MLP_OK;
+}
+
+// Dropout parameters from p in [0, 1): keep when the top 24 bits of the element's Philox
+// word are >= floor(p * 2^24); kept values are scaled by 1 / (1 - p).
+static bool make_dropout(double p, unsigned long long seed, unsigned long long offset, DropoutParams* d)
+{
+    if (!(p >= 0.0 && p < 1.0)) return false;
+    d->seed = seed;
+    d->offset = offset;
+    d->p24 = static_cast<uint32_t>(std::floor(p * 16777216.0));
+    d->scale = static_cast<float>(1.0 / (1.0 - p));
+    return true;
+}
+
+}  // namespace mlp
+
+extern "C" {
+
+mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
+                          const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* G,
+                          mlp_bf16* Y, void* cuda_stream)
+{
+    return forward_impl(X, A, a, B, b, nullptr, nullptr, T, h, f, t, H, G, Y, cuda_stream);
+}
+
+mlp_status mlp_tp_forward_residual_dropout(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
+                                           const mlp_bf16* B, const mlp_bf16* b, const mlp_bf16* R, int T, int h,
+                                           int f, int t, double p, unsigned long long seed,
+                                           unsigned long long offset, mlp_bf16* H, mlp_bf16* G, mlp_bf16* Z,
+                                           void* cuda_stream)
+{
+    DropoutParams d;
+    if (!make_dropout(p, seed, offset, &d)) return MLP_EINVAL;
+    return forward_impl(X, A, a, B, b, R, &d, T, h, f, t, H, G, Z, cuda_stream);
+}
+
+mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, unsigned long long seed,
+                                   unsigned long long offset, mlp_bf16* dY, void* cuda_stream)
+{
+    DropoutParams d;
+    if (!make_dropout(p, seed, offset, &d) || T < 0 || h < 8) return MLP_EINVAL;
+    if (h % 8 != 0) return MLP_ESHAPE;
+    if (T > 0 && (!dZ || !dY)) return MLP_EINVAL;
+    if (!aligned16(dZ) || !aligned16(dY)) return MLP_EALIGN;
+    DeviceInfo* dev = nullptr;
+    mlp_status st = device_info(&dev);
+    if (st != MLP_OK) return st;
+    if (T == 0) return MLP_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    CallTimer timer(s);
+    const long long n8 = static_cast<long long>(T) * h / 8;
+    long long blocks = (n8 + 255) / 256;
+    const long long cap = static_cast<long long>(dev->num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    dropout_backward_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(dZ), n8, d,
+                                                                      reinterpret_cast<__nv_bfloat16*>(dY));
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_DROPOUT_BWD);
     return MLP_OK;
 }
 
@@ -479,7 +555,7 @@ const char* mlp_tp_kernel_name(int kernel)
     static const char* names[MLP_NUM_KERNELS] = {
         "gemm_fwd_up (H=XA+a, G=GELU(H))", "gemm_fwd_down (Y=GB+b)", "gemm_bwd_dh (dH=dY B^T * GELU'(H))",
         "gemm_bwd_dx (dX=dH A^T)",          "gemm_bwd_da (dA=X^T dH)", "gemm_bwd_db (dB=G^T dY)",
-        "colsum_partial (db)",              "bias_grad_finalize (da, db)"};
+        "colsum_partial (db)",              "bias_grad_finalize (da, db)", "dropout_backward (dY)"};
     return (kernel >= 0 && kernel < MLP_NUM_KERNELS) ? names[kernel] : "unknown";
 }
 

@@ -18,6 +18,8 @@
 // Epilogues (the step of the MLP block each one implements):
 //   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H)            -> stores H and G
 //   EPI_BIAS       Y = acc + b[n]                          -> stores Y
+//   EPI_BIAS_DROPOUT_RES  Z = R[m,n] + keep(m,n) (acc + b[n]) / (1 - p)   -> stores Z
+//                  (keep from Philox4x32-10 on the element's index; philox.cuh)
 //   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH (and, optionally,
 //                  its column sums over each 32-row block in fp32, for the bias gradient)
 //   EPI_PLAIN      D = acc                                 -> stores D
@@ -29,6 +31,7 @@
 #include <cstdint>
 
 #include "gemm_args.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mlp {
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
             uint4 hnext[4];
-            if (EPI == EPI_DGELU) {
+            if (EPI == EPI_DGELU || EPI == EPI_BIAS_DROPOUT_RES) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int n = n0 + 8 * i;
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 uint32_t p0[16], p1[16];
-                if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) {
+                if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_DROPOUT_RES) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         float bv[8];
@@ -448,6 +451,29 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                         unpack_bf16x8(u, bv);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) v[8 * i + j] += bv[j];
+                    }
+                }
+                if (EPI == EPI_BIAS_DROPOUT_RES) {
+                    float rv[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], rv + 8 * i);
+                    if (c + 1 < BN / 32) {  // prefetch the next chunk of the residual
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int n = nc + 32 + 8 * i;
+                            hnext[i] = (row < M && n < N)
+                                           ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
+                                           : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    // element index of column nc of this row; a multiple of 4 (N % 8 == 0)
+                    const unsigned long long q0 = (static_cast<unsigned long long>(row) * N + nc) >> 2;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint32_t kb = dropout_keep4(args.drop, q0 + g);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            v[4 * g + w] = rv[4 * g + w] + (((kb >> w) & 1u) ? v[4 * g + w] * args.drop.scale : 0.0f);
                     }
                 }
                 if (EPI == EPI_DGELU) {
