@@ -65,6 +65,16 @@ def _load():
             lib.oracle_residual_dropout.argtypes = [i64, i64, ctypes.c_double, dp, dp, dp, dp]
             lib.oracle_dropout_backward.restype = i32
             lib.oracle_dropout_backward.argtypes = [i64, i64, ctypes.c_double, dp, dp, dp]
+            lib.oracle_silu.restype = ctypes.c_double
+            lib.oracle_silu.argtypes = [ctypes.c_double]
+            lib.oracle_silu_grad.restype = ctypes.c_double
+            lib.oracle_silu_grad.argtypes = [ctypes.c_double]
+            lib.oracle_swiglu_forward.restype = i32
+            lib.oracle_swiglu_forward.argtypes = [i64, i64, i64] + [dp] * 8
+            lib.oracle_swiglu_backward.restype = i32
+            lib.oracle_swiglu_backward.argtypes = [i64, i64, i64] + [dp] * 12
+            lib.oracle_swiglu_sharded.restype = i32
+            lib.oracle_swiglu_sharded.argtypes = [i64, i64, i64, i64] + [dp] * 12
             _lib = lib
     return _lib
 
@@ -245,3 +255,54 @@ def fwd_bwd_residual_dropout(inp: dict, R, dZ, p: float, seed: int, offset: int 
     out = backward(inp["X"], inp["A"], inp["B"], H, G, dY, act)
     out.update(H=H, G=G, Y=Y, Z=Z, keep=keep, dY=dY, dR=_f64(dZ))
     return out
+
+
+# ---- SwiGLU variant: Y = (SiLU(X A) * X Wg) B ---------------------------------------------
+
+def silu(x) -> np.ndarray:
+    lib = _load()
+    xs = _f64(x)
+    return np.array([lib.oracle_silu(float(v)) for v in xs.ravel()]).reshape(xs.shape)
+
+
+def silu_grad(x) -> np.ndarray:
+    lib = _load()
+    xs = _f64(x)
+    return np.array([lib.oracle_silu_grad(float(v)) for v in xs.ravel()]).reshape(xs.shape)
+
+
+def swiglu_fwd_bwd(inp: dict) -> dict:
+    """Ha, Hg, U, Y and dX, dA, dWg, dB of the SwiGLU block (inputs X, A, Wg, B, dY)."""
+    lib = _load()
+    X, A, Wg, B, dY = (_f64(inp[k]) for k in ("X", "A", "Wg", "B", "dY"))
+    T, h = X.shape
+    f = A.shape[1]
+    o = {k: np.empty((T, f)) for k in ("Ha", "Hg", "U")}
+    o["Y"] = np.empty((T, h))
+    rc = lib.oracle_swiglu_forward(T, h, f, _p(X), _p(A), _p(Wg), _p(B), _p(o["Ha"]), _p(o["Hg"]), _p(o["U"]),
+                                   _p(o["Y"]))
+    assert rc == 0, rc
+    o.update(dX=np.empty((T, h)), dA=np.empty((h, f)), dWg=np.empty((h, f)), dB=np.empty((f, h)))
+    rc = lib.oracle_swiglu_backward(T, h, f, _p(X), _p(A), _p(Wg), _p(B), _p(o["Ha"]), _p(o["Hg"]), _p(o["U"]),
+                                    _p(dY), _p(o["dX"]), _p(o["dA"]), _p(o["dWg"]), _p(o["dB"]))
+    assert rc == 0, rc
+    return o
+
+
+def swiglu_sharded(inp: dict, t: int, parts: bool = False) -> dict:
+    lib = _load()
+    X, A, Wg, B, dY = (_f64(inp[k]) for k in ("X", "A", "Wg", "B", "dY"))
+    T, h = X.shape
+    f = A.shape[1]
+    o = {"Y": np.empty((T, h)), "dX": np.empty((T, h)), "dA": np.empty((h, f)), "dWg": np.empty((h, f)),
+         "dB": np.empty((f, h))}
+    Yp = np.empty((t, T, h)) if parts else None
+    dXp = np.empty((t, T, h)) if parts else None
+    rc = lib.oracle_swiglu_sharded(T, h, f, t, _p(X), _p(A), _p(Wg), _p(B), _p(dY), _p(o["Y"]), _p(o["dX"]),
+                                   _p(o["dA"]), _p(o["dWg"]), _p(o["dB"]), _p(Yp) if parts else None,
+                                   _p(dXp) if parts else None)
+    if rc != 0:
+        raise ValueError(f"oracle_swiglu_sharded rejected f={f} t={t}")
+    if parts:
+        o["Y_part"], o["dX_part"] = Yp, dXp
+    return o

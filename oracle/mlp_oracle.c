@@ -468,3 +468,103 @@ int oracle_dropout_backward(int64_t T, int64_t h, double p, const double *dZ, co
     for (int64_t e = 0; e < T * h; ++e) dY[e] = keep[e] ? dZ[e] * scale : 0.0;
     return 0;
 }
+
+/* ---- SwiGLU variant of the block ----------------------------------------------------- */
+
+/* "Distributed training" (ml-interview-book), section 7 "Exercises", exercise 3: the SwiGLU
+ * MLP Y = (SiLU(X A) (.) X Wg) B with A and Wg both split by columns and B by rows; each
+ * shard's SiLU and product are shard-local, so Y = sum_i (SiLU(X A_i) (.) X Wg_i) B_i and
+ * one sum remains. No biases, as on the page. SiLU(x) = x sigma(x). */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double silu(double x) { return x * sigmoid(x); }
+/* d/dx x sigma(x) = sigma(x) + x sigma(x) (1 - sigma(x)) */
+static double silu_grad(double x)
+{
+    double s = sigmoid(x);
+    return s + x * s * (1.0 - s);
+}
+
+double oracle_silu(double x) { return silu(x); }
+double oracle_silu_grad(double x) { return silu_grad(x); }
+
+/* Ha = X A, Hg = X Wg, U = SiLU(Ha) (.) Hg, Y = U B. */
+int oracle_swiglu_forward(int64_t T, int64_t h, int64_t f, const double *X, const double *A, const double *Wg,
+                          const double *B, double *Ha, double *Hg, double *U, double *Y)
+{
+    if (T < 0 || h < 1 || f < 1) return 1;
+    mm_nn(T, f, h, X, A, Ha);
+    mm_nn(T, f, h, X, Wg, Hg);
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < T * f; ++e) U[e] = silu(Ha[e]) * Hg[e];
+    mm_nn(T, h, f, U, B, Y);
+    return 0;
+}
+
+/* Chain rule: dU = dY B^T; dHa = dU (.) Hg (.) SiLU'(Ha); dHg = dU (.) SiLU(Ha);
+ * dX = dHa A^T + dHg Wg^T; dA = X^T dHa; dWg = X^T dHg; dB = U^T dY. */
+int oracle_swiglu_backward(int64_t T, int64_t h, int64_t f, const double *X, const double *A, const double *Wg,
+                           const double *B, const double *Ha, const double *Hg, const double *U, const double *dY,
+                           double *dX, double *dA, double *dWg, double *dB)
+{
+    if (T < 0 || h < 1 || f < 1) return 1;
+    size_t n = (size_t)(T * f > 0 ? T * f : 1);
+    double *dU = malloc(sizeof(double) * n), *dHa = malloc(sizeof(double) * n), *dHg = malloc(sizeof(double) * n);
+    double *dX2 = malloc(sizeof(double) * (size_t)(T * h > 0 ? T * h : 1));
+    if (!dU || !dHa || !dHg || !dX2) return 2;
+    mm_nt(T, f, h, dY, B, dU);
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < T * f; ++e) {
+        dHa[e] = dU[e] * Hg[e] * silu_grad(Ha[e]);
+        dHg[e] = dU[e] * silu(Ha[e]);
+    }
+    mm_nt(T, h, f, dHa, A, dX);
+    mm_nt(T, h, f, dHg, Wg, dX2);
+    for (int64_t e = 0; e < T * h; ++e) dX[e] += dX2[e];
+    mm_tn(h, f, T, X, dHa, dA);
+    mm_tn(h, f, T, X, dHg, dWg);
+    mm_tn(f, h, T, U, dY, dB);
+    free(dU); free(dHa); free(dHg); free(dX2);
+    return 0;
+}
+
+/* Shard by shard, with the explicit sums over shards of the partial outputs (forward) and
+ * of the partial input gradients (backward); Y_part, dX_part (optional) get [t,T,h]. */
+int oracle_swiglu_sharded(int64_t T, int64_t h, int64_t f, int64_t t, const double *X, const double *A,
+                          const double *Wg, const double *B, const double *dY, double *Y, double *dX, double *dA,
+                          double *dWg, double *dB, double *Y_part, double *dX_part)
+{
+    if (T < 0 || h < 1 || f < 1 || t < 1 || f % t != 0) return 1;
+    int64_t fs = f / t;
+    size_t nhf = (size_t)(h * fs), nTf = (size_t)(T * fs > 0 ? T * fs : 1), nTh = (size_t)(T * h > 0 ? T * h : 1);
+    double *Ai = malloc(sizeof(double) * nhf), *Wi = malloc(sizeof(double) * nhf), *Bi = malloc(sizeof(double) * nhf);
+    double *Ha = malloc(sizeof(double) * nTf), *Hg = malloc(sizeof(double) * nTf), *U = malloc(sizeof(double) * nTf);
+    double *P = malloc(sizeof(double) * nTh), *dXi = malloc(sizeof(double) * nTh);
+    double *dAi = malloc(sizeof(double) * nhf), *dWi = malloc(sizeof(double) * nhf), *dBi = malloc(sizeof(double) * nhf);
+    if (!Ai || !Wi || !Bi || !Ha || !Hg || !U || !P || !dXi || !dAi || !dWi || !dBi) return 2;
+    for (int64_t i = 0; i < T * h; ++i) { Y[i] = 0.0; dX[i] = 0.0; }
+    for (int64_t s = 0; s < t; ++s) {
+        int64_t c0 = s * fs;
+        for (int64_t k = 0; k < h; ++k)
+            for (int64_t j = 0; j < fs; ++j) {
+                Ai[k * fs + j] = A[k * f + c0 + j];
+                Wi[k * fs + j] = Wg[k * f + c0 + j];
+            }
+        for (int64_t j = 0; j < fs; ++j)
+            for (int64_t n = 0; n < h; ++n) Bi[j * h + n] = B[(c0 + j) * h + n];
+        oracle_swiglu_forward(T, h, fs, X, Ai, Wi, Bi, Ha, Hg, U, P);
+        for (int64_t i = 0; i < T * h; ++i) Y[i] += P[i];
+        if (Y_part) memcpy(Y_part + s * T * h, P, sizeof(double) * (size_t)(T * h));
+        oracle_swiglu_backward(T, h, fs, X, Ai, Wi, Bi, Ha, Hg, U, dY, dXi, dAi, dWi, dBi);
+        for (int64_t i = 0; i < T * h; ++i) dX[i] += dXi[i];
+        if (dX_part) memcpy(dX_part + s * T * h, dXi, sizeof(double) * (size_t)(T * h));
+        for (int64_t k = 0; k < h; ++k)
+            for (int64_t j = 0; j < fs; ++j) {
+                dA[k * f + c0 + j] = dAi[k * fs + j];
+                dWg[k * f + c0 + j] = dWi[k * fs + j];
+            }
+        for (int64_t j = 0; j < fs; ++j)
+            for (int64_t n = 0; n < h; ++n) dB[(c0 + j) * h + n] = dBi[j * h + n];
+    }
+    free(Ai); free(Wi); free(Bi); free(Ha); free(Hg); free(U); free(P); free(dXi); free(dAi); free(dWi); free(dBi);
+    return 0;
+}
