@@ -126,6 +126,31 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
 mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf16* dY, int T, int h, int f,
                                      float* da, float* db, void* cuda_stream);
 
+/* SwiGLU variant of the block ("Distributed training", ml-interview-book, section 7,
+ * exercise 3): Y = (SiLU(X A) (.) X Wg) B, with A and Wg both split by columns and B by
+ * rows into t shards (each shard's SiLU and product are shard-local; one sum remains, the
+ * K loop of the down-projection). No biases. SiLU(x) = x sigma(x).
+ *   X [T,h]  A, Wg [h,f]  B [f,h]  Ha, Hg, U [T,f]  Y [T,h]
+ * Forward: Ha = X A and Hg = X Wg come out of one GEMM (both halves of one 256-wide MMA per
+ * 128 output columns, sharing the X tiles) whose epilogue also writes U = SiLU(Ha) Hg; then
+ * Y = U B. Ha, Hg, U are kept for the backward. Two launches. */
+mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
+                                 const mlp_bf16* B, int T, int h, int f, int t, mlp_bf16* Ha,
+                                 mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* cuda_stream);
+
+/* SwiGLU backward given dY: dU = dY B^T; dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha) (in the
+ * dU GEMM's epilogue); dX = dHa A^T + dHg Wg^T (one accumulator over both K segments);
+ * dA = X^T dHa; dWg = X^T dHg; dB = U^T dY. `workspace` (>= mlp_tp_swiglu_workspace_bytes(),
+ * 256-byte aligned) holds dHa and dHg. Five launches. */
+mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
+                                  const mlp_bf16* B, const mlp_bf16* Ha, const mlp_bf16* Hg,
+                                  const mlp_bf16* U, const mlp_bf16* dY, int T, int h, int f, int t,
+                                  mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dWg, mlp_bf16* dB,
+                                  void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Device bytes mlp_tp_swiglu_backward needs as workspace (0 on invalid sizes). */
+size_t mlp_tp_swiglu_workspace_bytes(int T, int h, int f, int t);
+
 /* Device bytes mlp_tp_backward needs as workspace for these sizes (0 on invalid sizes). */
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
 

@@ -76,6 +76,12 @@ def lib() -> ctypes.CDLL:
                                                           [vp] * 3 + [vp])
             L.mlp_tp_dropout_backward.restype = i32
             L.mlp_tp_dropout_backward.argtypes = [vp, i32, i32, ctypes.c_double, u64, u64, vp, vp]
+            L.mlp_tp_swiglu_forward.restype = i32
+            L.mlp_tp_swiglu_forward.argtypes = [vp] * 4 + [i32] * 4 + [vp] * 4 + [vp]
+            L.mlp_tp_swiglu_backward.restype = i32
+            L.mlp_tp_swiglu_backward.argtypes = [vp] * 8 + [i32] * 4 + [vp] * 5 + [sz, vp]
+            L.mlp_tp_swiglu_workspace_bytes.restype = sz
+            L.mlp_tp_swiglu_workspace_bytes.argtypes = [i32] * 4
             L.mlp_tp_bias_grads_noalloc.restype = i32
             L.mlp_tp_bias_grads_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
             _lib = L
@@ -185,3 +191,19 @@ def mlp_tp_forward_residual_dropout(X, A, a, B, b, R, T: int, h: int, f: int, t:
 def mlp_tp_dropout_backward(dZ, T: int, h: int, p: float, seed: int, offset: int, dY, stream=None) -> None:
     _check(lib().mlp_tp_dropout_backward(_ptr(dZ), T, h, float(p), int(seed), int(offset), _ptr(dY),
                                          _stream(stream)), "mlp_tp_dropout_backward")
+
+
+def mlp_tp_swiglu_forward(X, A, Wg, B, T: int, h: int, f: int, t: int, Ha, Hg, U, Y, stream=None) -> None:
+    _check(lib().mlp_tp_swiglu_forward(_ptr(X), _ptr(A), _ptr(Wg), _ptr(B), T, h, f, t, _ptr(Ha), _ptr(Hg),
+                                       _ptr(U), _ptr(Y), _stream(stream)), "mlp_tp_swiglu_forward")
+
+
+def mlp_tp_swiglu_backward(X, A, Wg, B, Ha, Hg, U, dY, T: int, h: int, f: int, t: int, dX, dA, dWg, dB,
+                           workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib().mlp_tp_swiglu_backward(_ptr(X), _ptr(A), _ptr(Wg), _ptr(B), _ptr(Ha), _ptr(Hg), _ptr(U), _ptr(dY),
+                                        T, h, f, t, _ptr(dX), _ptr(dA), _ptr(dWg), _ptr(dB), _ptr(workspace),
+                                        workspace_bytes, _stream(stream)), "mlp_tp_swiglu_backward")
+
+
+def mlp_tp_swiglu_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
+    return int(lib().mlp_tp_swiglu_workspace_bytes(T, h, f, t))

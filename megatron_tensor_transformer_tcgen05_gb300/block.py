@@ -49,3 +49,29 @@ def step(inp: dict, buf: dict, t: int, stream=None) -> None:
     """One forward + backward of the block."""
     forward(inp, buf, t, stream)
     backward(inp, buf, t, stream)
+
+
+# ---- SwiGLU variant -----------------------------------------------------------------------
+
+def empty_swiglu_buffers(T: int, h: int, f: int, t: int, device="cuda") -> dict[str, torch.Tensor]:
+    from ._lib import mlp_tp_swiglu_workspace_bytes
+    bf = torch.bfloat16
+    ws = mlp_tp_swiglu_workspace_bytes(T, h, f, t)
+    if ws == 0:
+        raise ValueError(f"invalid sizes T={T} h={h} f={f} t={t}")
+    out = {k: torch.empty((T, f), dtype=bf, device=device) for k in ("Ha", "Hg", "U")}
+    out.update(Y=torch.empty((T, h), dtype=bf, device=device), dX=torch.empty((T, h), dtype=bf, device=device),
+               dA=torch.empty((h, f), dtype=bf, device=device), dWg=torch.empty((h, f), dtype=bf, device=device),
+               dB=torch.empty((f, h), dtype=bf, device=device), ws=torch.empty((ws,), dtype=torch.uint8, device=device))
+    return out
+
+
+def swiglu_step(inp: dict, buf: dict, t: int, stream=None) -> None:
+    """One forward + backward of the SwiGLU block."""
+    from ._lib import mlp_tp_swiglu_backward, mlp_tp_swiglu_forward
+    T, h = inp["X"].shape
+    f = inp["A"].shape[1]
+    mlp_tp_swiglu_forward(inp["X"], inp["A"], inp["Wg"], inp["B"], T, h, f, t, buf["Ha"], buf["Hg"], buf["U"],
+                          buf["Y"], stream)
+    mlp_tp_swiglu_backward(inp["X"], inp["A"], inp["Wg"], inp["B"], buf["Ha"], buf["Hg"], buf["U"], inp["dY"], T, h,
+                           f, t, buf["dX"], buf["dA"], buf["dWg"], buf["dB"], buf["ws"], buf["ws"].numel(), stream)

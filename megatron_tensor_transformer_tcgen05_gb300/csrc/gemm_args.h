@@ -8,13 +8,24 @@
 
 namespace mlp {
 
-enum Epi : int { EPI_PLAIN = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2, EPI_DGELU = 3, EPI_BIAS_DROPOUT_RES = 4 };
+enum Epi : int {
+    EPI_PLAIN = 0,
+    EPI_BIAS = 1,
+    EPI_BIAS_GELU = 2,
+    EPI_DGELU = 3,
+    EPI_BIAS_DROPOUT_RES = 4,
+    EPI_SWIGLU = 5,   // dual B operand: D = [X A | X Wg] per 128 output columns -> Ha, Hg, U
+    EPI_DSWIGLU = 6,  // dU = acc; dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha) -> dHa, dHg
+};
 
 struct GemmArgs {
     CUtensorMap tmA;    // A operand (K-major box 64x128, or MN-major box 64x64)
     CUtensorMap tmB;    // B operand (K-major box 64xBN, or MN-major box 64x64)
     CUtensorMap tmD0;   // first output, store box 32x32, 64B swizzle
     CUtensorMap tmD1;   // second output (G of EPI_BIAS_GELU), same box
+    CUtensorMap tmD2;   // third output (U of EPI_SWIGLU), same box
+    CUtensorMap tmA2;   // A operand of the second K segment (kb_split > 0)
+    CUtensorMap tmB2;   // B operand of the second K segment, or the gate weight of EPI_SWIGLU
     int M, N, K;
     int n_fastest;               // tile order: 0 = M index fastest, 1 = N index fastest
     int raster_group;            // tiles of the fast index per group (<= 0: all of them)
@@ -22,7 +33,11 @@ struct GemmArgs {
     const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU; residual R for EPI_BIAS_DROPOUT_RES
     float* colsum_rows;          // EPI_DGELU, optional: per-32-row column sums of D (fp32),
                                  // [ceil(M/32), N] row-major; NULL = not wanted
+    const __nv_bfloat16* aux2;   // Hg [M, ld_aux] for EPI_DSWIGLU (aux is Ha)
     long long ld_aux;
+    // K concatenation: k blocks [0, kb_split) read (tmA, tmB), the rest read (tmA2, tmB2)
+    // from their own k = 0, so D = A1 B1^T + A2 B2^T in one accumulator (0 = one segment).
+    int kb_split;
     int* status;                 // device status word (first error code wins)
     DropoutParams drop;          // EPI_BIAS_DROPOUT_RES
     unsigned long long timeout_ns;

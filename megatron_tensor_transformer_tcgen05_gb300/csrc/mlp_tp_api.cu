@@ -148,6 +148,20 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
                      : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, grid, s);
 }
 
+// The SwiGLU up-projection: one 256-wide MMA per 128 output columns ([X A | X Wg]).
+static cudaError_t gemm_dual(GemmArgs& g, int num_sms, cudaStream_t s)
+{
+    g.n_fastest = g.M > g.N ? 1 : 0;
+    const bool pair = g.M > 128;
+    const int units = pair ? num_sms / 2 : num_sms;
+    g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(units > 1 ? units : 1))));
+    const long long tiles = static_cast<long long>((g.M + (pair ? 255 : 127)) / (pair ? 256 : 128)) * ((g.N + 127) / 128);
+    const int grid_units = static_cast<int>(tiles < units ? tiles : units);
+    if (grid_units <= 0) return cudaSuccess;
+    return pair ? launch_umma_gemm<256, false, true, EPI_SWIGLU, 2>(g, 2 * grid_units, s)
+                : launch_umma_gemm<256, false, true, EPI_SWIGLU, 1>(g, grid_units, s);
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static mlp_status check_shape(int T, int h, int f, int t)
@@ -588,6 +602,139 @@ extern "C" mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, 
     if (limit_ns > 10000000000ull) return MLP_EINVAL;
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(dev->status, limit_ns);
     return cudaGetLastError() == cudaSuccess ? MLP_OK : MLP_ECUDA;
+}
+
+// ---- SwiGLU variant of the block ----------------------------------------------------------
+
+extern "C" size_t mlp_tp_swiglu_workspace_bytes(int T, int h, int f, int t)
+{
+    if (check_shape(T, h, f, t) != MLP_OK) return 0;
+    return 2 * round256(static_cast<size_t>(T) * f * 2);  // dHa, dHg
+}
+
+extern "C" mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
+                                            const mlp_bf16* B, int T, int h, int f, int t, mlp_bf16* Ha,
+                                            mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* cuda_stream)
+{
+    mlp_status st = check_shape(T, h, f, t);
+    if (st != MLP_OK) return st;
+    if (!A || !Wg || !B || (T > 0 && (!X || !Ha || !Hg || !U || !Y))) return MLP_EINVAL;
+    const void* ptrs[] = {X, A, Wg, B, Ha, Hg, U, Y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    if (T == 0) return MLP_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    CallTimer timer(s);
+
+    // Up-projection, both halves at once: Ha = X A, Hg = X Wg, U = SiLU(Ha) Hg.
+    GemmArgs g1{};
+    if (!map_kmajor(&g1.tmA, X, h, T, 128) || !map_mnmajor(&g1.tmB, A, f, h) || !map_mnmajor(&g1.tmB2, Wg, f, h) ||
+        !map_store(&g1.tmD0, Ha, f, T) || !map_store(&g1.tmD1, Hg, f, T) || !map_store(&g1.tmD2, U, f, T))
+        return MLP_ECUDA;
+    g1.M = T; g1.N = f; g1.K = h;
+    g1.status = dev->status;
+    g1.timeout_ns = kWaitLimitNs;
+    if (gemm_dual(g1, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_FWD_UP);
+
+    // Down-projection: Y = U B, the shard sum in one accumulator over K = f.
+    GemmArgs g2{};
+    if (!map_kmajor(&g2.tmA, U, f, T, 128) || !map_mnmajor(&g2.tmB, B, h, f) || !map_store(&g2.tmD0, Y, h, T))
+        return MLP_ECUDA;
+    g2.M = T; g2.N = h; g2.K = f;
+    g2.status = dev->status;
+    g2.timeout_ns = kWaitLimitNs;
+    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_FWD_DOWN);
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
+                                             const mlp_bf16* B, const mlp_bf16* Ha, const mlp_bf16* Hg,
+                                             const mlp_bf16* U, const mlp_bf16* dY, int T, int h, int f, int t,
+                                             mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dWg, mlp_bf16* dB,
+                                             void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    mlp_status st = check_shape(T, h, f, t);
+    if (st != MLP_OK) return st;
+    if (!A || !Wg || !B || !dA || !dWg || !dB || !workspace ||
+        (T > 0 && (!X || !Ha || !Hg || !U || !dY || !dX)))
+        return MLP_EINVAL;
+    const void* ptrs[] = {X, A, Wg, B, Ha, Hg, U, dY, dX, dA, dWg, dB};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
+    if (workspace_bytes < mlp_tp_swiglu_workspace_bytes(T, h, f, t)) return MLP_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (T == 0) {
+        const size_t w = static_cast<size_t>(h) * f * 2;
+        if (cudaMemsetAsync(dA, 0, w, s) != cudaSuccess || cudaMemsetAsync(dWg, 0, w, s) != cudaSuccess ||
+            cudaMemsetAsync(dB, 0, w, s) != cudaSuccess)
+            return MLP_ECUDA;
+        return MLP_OK;
+    }
+    const int bn_f = tile_n(f / t), bn_h = tile_n(h);
+    mlp_bf16* dHa = static_cast<mlp_bf16*>(workspace);
+    mlp_bf16* dHg = reinterpret_cast<mlp_bf16*>(static_cast<uint8_t*>(workspace) + round256(static_cast<size_t>(T) * f * 2));
+    CallTimer timer(s);
+
+    // dU = dY B^T, and in the epilogue dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha).
+    GemmArgs g3{};
+    if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, kmajor_b_box(T, bn_f)) ||
+        !map_store(&g3.tmD0, dHa, f, T) || !map_store(&g3.tmD1, dHg, f, T))
+        return MLP_ECUDA;
+    g3.M = T; g3.N = f; g3.K = h;
+    g3.aux = reinterpret_cast<const __nv_bfloat16*>(Ha);
+    g3.aux2 = reinterpret_cast<const __nv_bfloat16*>(Hg);
+    g3.ld_aux = f;
+    g3.status = dev->status;
+    g3.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_DSWIGLU>(g3, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DH);
+
+    // dX = dHa A^T + dHg Wg^T: one accumulator over the two K segments (the shard sum of
+    // both column-split weights at once).
+    GemmArgs g4{};
+    if (!map_kmajor(&g4.tmA, dHa, f, T, 128) || !map_kmajor(&g4.tmB, A, f, h, kmajor_b_box(T, bn_h)) ||
+        !map_kmajor(&g4.tmA2, dHg, f, T, 128) || !map_kmajor(&g4.tmB2, Wg, f, h, kmajor_b_box(T, bn_h)) ||
+        !map_store(&g4.tmD0, dX, h, T))
+        return MLP_ECUDA;
+    const int kb_f = (f + 63) / 64;
+    g4.M = T; g4.N = h; g4.K = 2 * 64 * kb_f;
+    g4.kb_split = kb_f;
+    g4.status = dev->status;
+    g4.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DX);
+
+    // dA = X^T dHa and dWg = X^T dHg.
+    const mlp_bf16* dHs[2] = {dHa, dHg};
+    mlp_bf16* dWs[2] = {dA, dWg};
+    for (int i = 0; i < 2; ++i) {
+        GemmArgs g5{};
+        if (!map_mnmajor(&g5.tmA, X, h, T) || !map_mnmajor(&g5.tmB, dHs[i], f, T) || !map_store(&g5.tmD0, dWs[i], f, h))
+            return MLP_ECUDA;
+        g5.M = h; g5.N = f; g5.K = T;
+        g5.status = dev->status;
+        g5.timeout_ns = kWaitLimitNs;
+        if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+        timer.mark(MLP_K_BWD_DA);
+    }
+
+    // dB = U^T dY.
+    GemmArgs g6{};
+    if (!map_mnmajor(&g6.tmA, U, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) || !map_store(&g6.tmD0, dB, h, f))
+        return MLP_ECUDA;
+    g6.M = f; g6.N = h; g6.K = T;
+    g6.status = dev->status;
+    g6.timeout_ns = kWaitLimitNs;
+    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_BWD_DB);
+    return MLP_OK;
 }
 
 // ---- bias gradients with no device allocation --------------------------------------------

@@ -23,6 +23,8 @@
 //   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH (and, optionally,
 //                  its column sums over each 32-row block in fp32, for the bias gradient)
 //   EPI_PLAIN      D = acc                                 -> stores D
+//   EPI_SWIGLU     acc = [X A | X Wg] over 128 columns: Ha, Hg, U = SiLU(Ha) Hg -> stores all three
+//   EPI_DSWIGLU    dU = acc: dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha)            -> stores both
 // GELU is the tanh form 0.5 x (1 + tanh u), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated
 // through the identity 1 + tanh u = 2 / (1 + exp(-2u)), which stays accurate where
 // 1 + tanh u is small.
@@ -44,16 +46,22 @@ struct GemmCfg {
     static constexpr int CG = CG_;
     static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int BN_CTA = BN / CG;  // rows of the B operand one CTA loads
-    static constexpr int STAGES = (CG == 2) ? 6 : 4;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
     static constexpr int EPI = EPI_;
+    // Dual B operand (SwiGLU up-projection): each tile covers OBN = BN/2 output columns,
+    // its MMA N = BN spans [A's columns | Wg's columns] of that range.
+    static constexpr bool DUAL = (EPI == EPI_SWIGLU);
+    static constexpr int OBN = DUAL ? BN / 2 : BN;
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int NOUT = (EPI == EPI_BIAS_GELU) ? 2 : 1;
+    static constexpr int NOUT = (EPI == EPI_SWIGLU) ? 3 : (EPI == EPI_BIAS_GELU || EPI == EPI_DSWIGLU) ? 2 : 1;
     static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
     static constexpr uint32_t EPI_BYTES = 4 * 2 * NOUT * STG_BYTES;  // 4 warps x 2 buffers
     static constexpr uint32_t TMEM_COLS = 2 * BN;                    // two fp32 accumulators
+    // as many stages as fit beside the epilogue staging (at most 6 for pairs, 4 alone)
+    static constexpr int STAGES_FIT = static_cast<int>((232448u - 1024u - 256u - EPI_BYTES) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT < ((CG == 2) ? 6 : 4) ? STAGES_FIT : ((CG == 2) ? 6 : 4);
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
     static constexpr uint32_t BAR_BYTES = 8 * NUM_BARS + 16;
     static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -62,6 +70,8 @@ struct GemmCfg {
     static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256-wide tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(STAGES >= 3, "pipeline depth");
+    static_assert(!DUAL || (B_MN && BN == 256), "dual B operand: MN-major, 256-wide MMA");
 };
 
 // In-flight copies get this long to land after an abort before the CTA exits.
@@ -86,6 +96,16 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float x)
     const float s = __fdividef(1.0f, 1.0f + e);
     const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
     return fmaf(2.0f * x * s * (1.0f - s), du, s);
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// SiLU(x) = x sigma(x); SiLU'(x) = sigma(x) (1 + x (1 - sigma(x))).
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+__device__ __forceinline__ float silu_grad_f(float x)
+{
+    const float s = sigmoid_f(x);
+    return s * fmaf(x, 1.0f - s, 1.0f);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -205,7 +225,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
     const int M = args.M, N = args.N, K = args.K;
     const int TM = C::BM * CG;  // rows per tile
     const int tiles_m = (M + TM - 1) / TM;
-    const int tiles_n = (N + BN - 1) / BN;
+    const int tiles_n = (N + C::OBN - 1) / C::OBN;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (K + C::BK - 1) / C::BK;
     const unsigned long long limit = args.timeout_ns;
@@ -225,7 +245,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         tma_prefetch_desc(&args.tmA);
         tma_prefetch_desc(&args.tmB);
         tma_prefetch_desc(&args.tmD0);
-        if (C::NOUT == 2) tma_prefetch_desc(&args.tmD1);
+        if (C::NOUT >= 2) tma_prefetch_desc(&args.tmD1);
+        if (C::NOUT >= 3) tma_prefetch_desc(&args.tmD2);
+        if (C::DUAL || args.kb_split > 0) tma_prefetch_desc(&args.tmB2);
+        if (args.kb_split > 0) tma_prefetch_desc(&args.tmA2);
     }
     if (CG == 2) cluster_sync();  // the peer CTA is running before the collective allocation
     if (warp == 1) {
@@ -252,7 +275,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             bool ok = true;
             for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 int m0, n0;
-                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, BN, m0, n0);
+                tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
                 const int m_cta = m0 + C::BM * static_cast<int>(rank);
                 const int n_cta = n0 + C::BN_CTA * static_cast<int>(rank);
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -264,21 +287,30 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     const uint32_t sa = s_stages + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
                     const uint32_t fb = b_full + 8u * stage;
-                    const int k0 = kb * C::BK;
+                    // second K segment (kb_split > 0): its own operands, from their k = 0
+                    const bool seg2 = args.kb_split > 0 && kb >= args.kb_split;
+                    const int k0 = (seg2 ? kb - args.kb_split : kb) * C::BK;
+                    const CUtensorMap* tA = seg2 ? &args.tmA2 : &args.tmA;
+                    const CUtensorMap* tB = seg2 ? &args.tmB2 : &args.tmB;
                     if (CG == 1) {
                         mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
                         if (A_MN) {
-                            tma_load_2d(sa, &args.tmA, m_cta, k0, fb);
-                            tma_load_2d(sa + 8192u, &args.tmA, m_cta + 64, k0, fb);
+                            tma_load_2d(sa, tA, m_cta, k0, fb);
+                            tma_load_2d(sa + 8192u, tA, m_cta + 64, k0, fb);
                         } else {
-                            tma_load_2d(sa, &args.tmA, k0, m_cta, fb);
+                            tma_load_2d(sa, tA, k0, m_cta, fb);
                         }
-                        if (B_MN) {
+                        if (C::DUAL) {  // rows [0, BN/2): A's columns; [BN/2, BN): Wg's, same range
 #pragma unroll
                             for (int i = 0; i < C::BN_CTA / 64; ++i)
-                                tma_load_2d(sb + 8192u * i, &args.tmB, n_cta + 64 * i, k0, fb);
+                                tma_load_2d(sb + 8192u * i, i < C::BN_CTA / 128 ? &args.tmB : &args.tmB2,
+                                            n0 + 64 * (i % (C::BN_CTA / 128)), k0, fb);
+                        } else if (B_MN) {
+#pragma unroll
+                            for (int i = 0; i < C::BN_CTA / 64; ++i)
+                                tma_load_2d(sb + 8192u * i, tB, n_cta + 64 * i, k0, fb);
                         } else {
-                            tma_load_2d(sb, &args.tmB, k0, n_cta, fb);
+                            tma_load_2d(sb, tB, k0, n_cta, fb);
                         }
                     } else {
                         // Both CTAs' bytes complete on the even CTA's barrier, which the even
@@ -286,17 +318,22 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                         const uint32_t fb0 = mapa_shared(fb, 0);
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
                         if (A_MN) {
-                            tma_load_2d_pair(sa, &args.tmA, m_cta, k0, fb0);
-                            tma_load_2d_pair(sa + 8192u, &args.tmA, m_cta + 64, k0, fb0);
+                            tma_load_2d_pair(sa, tA, m_cta, k0, fb0);
+                            tma_load_2d_pair(sa + 8192u, tA, m_cta + 64, k0, fb0);
                         } else {
-                            tma_load_2d_pair(sa, &args.tmA, k0, m_cta, fb0);
+                            tma_load_2d_pair(sa, tA, k0, m_cta, fb0);
                         }
-                        if (B_MN) {
+                        if (C::DUAL) {  // the even CTA holds A's columns, the odd one Wg's
 #pragma unroll
                             for (int i = 0; i < C::BN_CTA / 64; ++i)
-                                tma_load_2d_pair(sb + 8192u * i, &args.tmB, n_cta + 64 * i, k0, fb0);
+                                tma_load_2d_pair(sb + 8192u * i, rank == 0 ? &args.tmB : &args.tmB2, n0 + 64 * i,
+                                                 k0, fb0);
+                        } else if (B_MN) {
+#pragma unroll
+                            for (int i = 0; i < C::BN_CTA / 64; ++i)
+                                tma_load_2d_pair(sb + 8192u * i, tB, n_cta + 64 * i, k0, fb0);
                         } else {
-                            tma_load_2d_pair(sb, &args.tmB, k0, n_cta, fb0);
+                            tma_load_2d_pair(sb, tB, k0, n_cta, fb0);
                         }
                     }
                     issued |= 1u << stage;
@@ -402,31 +439,34 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             if (!ready) break;
             tc_fence_after();
             int m0, n0;
-            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, BN, m0, n0);
+            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
             const int row_blk = m0 + C::BM * static_cast<int>(rank) + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
-            uint4 hnext[4];
-            if (EPI == EPI_DGELU || EPI == EPI_BIAS_DROPOUT_RES) {
+            uint4 hnext[4], gnext[4];
+            if (EPI == EPI_DGELU || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int n = n0 + 8 * i;
-                    hnext[i] = (row < M && n < N)
-                                   ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
-                                   : make_uint4(0, 0, 0, 0);
+                    const bool in = row < M && n < N;
+                    hnext[i] = in ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n) : make_uint4(0, 0, 0, 0);
+                    if (EPI == EPI_DSWIGLU)
+                        gnext[i] = in ? ldg_nc_v4(args.aux2 + static_cast<size_t>(row) * args.ld_aux + n)
+                                      : make_uint4(0, 0, 0, 0);
                 }
             }
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < C::OBN / 32; ++c) {
                 const int nc = n0 + 32 * c;
                 const bool active = nc < N;  // warp-uniform
-                uint32_t r[32];
+                uint32_t r[32], r2[32];
                 if (active) {
                     tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                    if (C::DUAL) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(C::OBN) + 32u * c, r2);  // X Wg
                     tmem_ld_wait();
                 }
-                if (c == BN / 32 - 1) {
+                if (c == C::OBN / 32 - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {  // accumulator may be reused
@@ -441,7 +481,40 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                uint32_t p0[16], p1[16];
+                uint32_t p0[16], p1[16], p2[16];
+                if (EPI == EPI_SWIGLU) {  // v = Ha = X A, r2 = Hg = X Wg: keep both, U = SiLU(Ha) Hg
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float ga = __uint_as_float(r2[2 * j]), gb = __uint_as_float(r2[2 * j + 1]);
+                        p1[j] = pack_bf16x2(ga, gb);
+                        p2[j] = pack_bf16x2(silu_f(v[2 * j]) * ga, silu_f(v[2 * j + 1]) * gb);
+                    }
+                }
+                if (EPI == EPI_DSWIGLU) {  // v = dU; dHa = dU Hg SiLU'(Ha) (in v), dHg = dU SiLU(Ha)
+                    float ha[32], hg[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        unpack_bf16x8(hnext[i], ha + 8 * i);
+                        unpack_bf16x8(gnext[i], hg + 8 * i);
+                    }
+                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of Ha and Hg
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int n = nc + 32 + 8 * i;
+                            const bool in = row < M && n < N;
+                            const size_t o = static_cast<size_t>(row) * args.ld_aux + n;
+                            hnext[i] = in ? ldg_nc_v4(args.aux + o) : make_uint4(0, 0, 0, 0);
+                            gnext[i] = in ? ldg_nc_v4(args.aux2 + o) : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float d0 = v[2 * j], d1 = v[2 * j + 1];
+                        p1[j] = pack_bf16x2(d0 * silu_f(ha[2 * j]), d1 * silu_f(ha[2 * j + 1]));
+                        v[2 * j] = d0 * hg[2 * j] * silu_grad_f(ha[2 * j]);
+                        v[2 * j + 1] = d1 * hg[2 * j + 1] * silu_grad_f(ha[2 * j + 1]);
+                    }
+                }
                 if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_DROPOUT_RES) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -457,7 +530,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     float rv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], rv + 8 * i);
-                    if (c + 1 < BN / 32) {  // prefetch the next chunk of the residual
+                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of the residual
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int n = nc + 32 + 8 * i;
@@ -480,7 +553,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
-                    if (c + 1 < BN / 32) {  // prefetch the next chunk of H
+                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of H
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int n = nc + 32 + 8 * i;
@@ -512,12 +585,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `sel` has read it
                 __syncwarp();
                 stage_row_sw64(buf0, lane, p0);
-                if (EPI == EPI_BIAS_GELU) stage_row_sw64(buf0 + C::STG_BYTES, lane, p1);
+                if (C::NOUT >= 2) stage_row_sw64(buf0 + C::STG_BYTES, lane, p1);
+                if (C::NOUT >= 3) stage_row_sw64(buf0 + 2 * C::STG_BYTES, lane, p2);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_2d(&args.tmD0, nc, row_blk, buf0);
-                    if (EPI == EPI_BIAS_GELU) tma_store_2d(&args.tmD1, nc, row_blk, buf0 + C::STG_BYTES);
+                    if (C::NOUT >= 2) tma_store_2d(&args.tmD1, nc, row_blk, buf0 + C::STG_BYTES);
+                    if (C::NOUT >= 3) tma_store_2d(&args.tmD2, nc, row_blk, buf0 + 2 * C::STG_BYTES);
                     bulk_commit_group();
                 }
                 sel ^= 1u;

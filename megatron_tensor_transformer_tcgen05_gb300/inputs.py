@@ -31,11 +31,13 @@ class Workload:
     sbias: float = 0.01  # std of a and b
     sdy: float = 0.01   # std of dY
     desc: str = ""
+    kind: str = "gelu"   # "gelu": Y = GELU(X A + a) B + b;  "swiglu": Y = (SiLU(X A) * X Wg) B
 
     @property
     def flops_fwd_bwd(self) -> int:
-        """Matmul FLOPs of one forward + backward: 6 GEMMs of 2*T*h*f each."""
-        return 12 * self.T * self.h * self.f
+        """Matmul FLOPs of one forward + backward: 6 GEMMs of 2*T*h*f each (GELU block), or
+        9 (SwiGLU block: X A, X Wg, U B; dU, dX over two K segments, dA, dWg, dB)."""
+        return (18 if self.kind == "swiglu" else 12) * self.T * self.h * self.f
 
 
 WORKLOADS: dict[str, Workload] = {w.name: w for w in [
@@ -51,6 +53,10 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
              desc="GPT-3 175B-shaped layer T=4096 (2x2048) h=12288 f=49152 t=8"),
     Workload("gpt-1t", 2048, 25600, 102400, 8, sw=0.006,
              desc="1T-shaped layer T=2048 (1x2048) h=25600 f=102400 t=8"),
+    # SwiGLU variant at the GPT-3 175B layer shape, f = 8h/3 so that its three weight
+    # matrices hold as many parameters as the GELU block's two.
+    Workload("gpt3-175b-swiglu", 4096, 12288, 32768, 8, kind="swiglu",
+             desc="SwiGLU MLP at the GPT-3 175B layer shape T=4096 h=12288 f=32768 (8h/3) t=8"),
 ]}
 
 NAMES = ("X", "A", "a", "B", "b", "dY")
@@ -85,3 +91,23 @@ def make_workload_inputs(w: Workload, *, seed: int = 0, rows: int | None = None
                          ) -> dict[str, torch.Tensor]:
     return make_inputs(w.T, w.h, w.f, seed=seed, sx=w.sx, sw=w.sw, sbias=w.sbias,
                        sdy=w.sdy, rows=rows)
+
+
+def make_swiglu_inputs(T: int, h: int, f: int, *, seed: int = 0, sx: float = 1.0, sw: float = 0.02,
+                       sdy: float = 0.01) -> dict[str, torch.Tensor]:
+    """Inputs of the SwiGLU block, drawn in the order X, A, Wg, B, dY (same recipe)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    shp = {"X": (T, h), "A": (h, f), "Wg": (h, f), "B": (f, h), "dY": (T, h)}
+    sig = {"X": sx, "A": sw, "Wg": sw, "B": sw, "dY": sdy}
+    out = {}
+    for name, s in shp.items():
+        v = torch.randn(s, generator=g, dtype=torch.float32)
+        v.mul_(sig[name])
+        out[name] = v.to(torch.bfloat16)
+    return out
+
+
+def make_any_inputs(w: Workload, *, seed: int = 0) -> dict[str, torch.Tensor]:
+    if w.kind == "swiglu":
+        return make_swiglu_inputs(w.T, w.h, w.f, seed=seed, sx=w.sx, sw=w.sw, sdy=w.sdy)
+    return make_workload_inputs(w, seed=seed)

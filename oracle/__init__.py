@@ -73,6 +73,8 @@ def _load():
             lib.oracle_swiglu_forward.argtypes = [i64, i64, i64] + [dp] * 8
             lib.oracle_swiglu_backward.restype = i32
             lib.oracle_swiglu_backward.argtypes = [i64, i64, i64] + [dp] * 12
+            lib.oracle_swiglu_sampled_bf16.restype = i32
+            lib.oracle_swiglu_sampled_bf16.argtypes = [i64, i64, i64] + [dp] * 5 + [i64, dp, i64, dp] + [dp] * 5
             lib.oracle_swiglu_sharded.restype = i32
             lib.oracle_swiglu_sharded.argtypes = [i64, i64, i64, i64] + [dp] * 12
             _lib = lib
@@ -306,3 +308,21 @@ def swiglu_sharded(inp: dict, t: int, parts: bool = False) -> dict:
     if parts:
         o["Y_part"], o["dX_part"] = Yp, dXp
     return o
+
+
+def swiglu_sampled_bf16(inp: dict, rows, cols) -> dict:
+    """Sampled entries of the SwiGLU block over bf16 inputs: Y_rows, dX_rows [nR,h];
+    dA_cols, dWg_cols [h,nC]; dB_rows [nC,h]."""
+    lib = _load()
+    X, A, Wg, B, dY = (_bits(inp[k]) for k in ("X", "A", "Wg", "B", "dY"))
+    T, h = X.shape
+    f = A.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    nR, nC = len(rows), len(cols)
+    Yr = np.empty((nR, h)); dXr = np.empty((nR, h)); dAc = np.empty((nC, h)); dWc = np.empty((nC, h))
+    dBc = np.empty((nC, h))
+    rc = lib.oracle_swiglu_sampled_bf16(T, h, f, _p(X), _p(A), _p(Wg), _p(B), _p(dY), nR, _p(rows), nC, _p(cols),
+                                        _p(Yr), _p(dXr), _p(dAc), _p(dWc), _p(dBc))
+    assert rc == 0, rc
+    return {"Y_rows": Yr, "dX_rows": dXr, "dA_cols": dAc.T.copy(), "dWg_cols": dWc.T.copy(), "dB_rows": dBc}

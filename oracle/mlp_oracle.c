@@ -568,3 +568,81 @@ int oracle_swiglu_sharded(int64_t T, int64_t h, int64_t f, int64_t t, const doub
     free(Ai); free(Wi); free(Bi); free(Ha); free(Hg); free(U); free(P); free(dXi); free(dAi); free(dWi); free(dBi);
     return 0;
 }
+
+/* The SwiGLU block evaluated only where asked, over bf16 inputs (as oracle_mlp_sampled_bf16):
+ * sampled tokens rows[i] -> Y[r,:], dX[r,:]; sampled columns cols[c] -> dA[:,j], dWg[:,j],
+ * dB[j,:]. Each entry is the full sum of its definition. */
+int oracle_swiglu_sampled_bf16(int64_t T, int64_t h, int64_t f, const uint16_t *X, const uint16_t *A,
+                               const uint16_t *Wg, const uint16_t *B, const uint16_t *dY, int64_t nR,
+                               const int64_t *rows, int64_t nC, const int64_t *cols, double *Yr, double *dXr,
+                               double *dAc, double *dWc, double *dBc)
+{
+    if (T < 1 || h < 1 || f < 1) return 1;
+    for (int64_t i = 0; i < nR; ++i) if (rows[i] < 0 || rows[i] >= T) return 1;
+    for (int64_t c = 0; c < nC; ++c) if (cols[c] < 0 || cols[c] >= f) return 1;
+#pragma omp parallel
+    {
+        double *x = malloc(sizeof(double) * (size_t)h), *dy = malloc(sizeof(double) * (size_t)h);
+        double *ha = malloc(sizeof(double) * (size_t)f), *hg = malloc(sizeof(double) * (size_t)f);
+        double *dha = malloc(sizeof(double) * (size_t)f), *dhg = malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nR; ++i) {
+            int64_t r = rows[i];
+            for (int64_t k = 0; k < h; ++k) { x[k] = bf16d(X[r * h + k]); dy[k] = bf16d(dY[r * h + k]); }
+            for (int64_t j = 0; j < f; ++j) { ha[j] = 0.0; hg[j] = 0.0; }
+            for (int64_t k = 0; k < h; ++k)
+                for (int64_t j = 0; j < f; ++j) {
+                    ha[j] += x[k] * bf16d(A[k * f + j]);
+                    hg[j] += x[k] * bf16d(Wg[k * f + j]);
+                }
+            for (int64_t n = 0; n < h; ++n) Yr[i * h + n] = 0.0;
+            for (int64_t j = 0; j < f; ++j) {
+                double u = silu(ha[j]) * hg[j], du = 0.0;
+                for (int64_t n = 0; n < h; ++n) {
+                    double bjn = bf16d(B[j * h + n]);
+                    Yr[i * h + n] += u * bjn;
+                    du += dy[n] * bjn;
+                }
+                dha[j] = du * hg[j] * silu_grad(ha[j]);
+                dhg[j] = du * silu(ha[j]);
+            }
+            for (int64_t k = 0; k < h; ++k) {
+                double s = 0.0;
+                for (int64_t j = 0; j < f; ++j) s += dha[j] * bf16d(A[k * f + j]) + dhg[j] * bf16d(Wg[k * f + j]);
+                dXr[i * h + k] = s;
+            }
+        }
+        free(x); free(dy); free(ha); free(hg); free(dha); free(dhg);
+    }
+#pragma omp parallel
+    {
+        double *ac = malloc(sizeof(double) * (size_t)h), *wc = malloc(sizeof(double) * (size_t)h);
+        double *br = malloc(sizeof(double) * (size_t)h);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t c = 0; c < nC; ++c) {
+            int64_t j = cols[c];
+            for (int64_t k = 0; k < h; ++k) { ac[k] = bf16d(A[k * f + j]); wc[k] = bf16d(Wg[k * f + j]); }
+            for (int64_t n = 0; n < h; ++n) br[n] = bf16d(B[j * h + n]);
+            for (int64_t k = 0; k < h; ++k) { dAc[c * h + k] = 0.0; dWc[c * h + k] = 0.0; }
+            for (int64_t n = 0; n < h; ++n) dBc[c * h + n] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                double a = 0.0, g = 0.0, du = 0.0;
+                for (int64_t k = 0; k < h; ++k) {
+                    double xv = bf16d(X[r * h + k]);
+                    a += xv * ac[k];
+                    g += xv * wc[k];
+                }
+                for (int64_t n = 0; n < h; ++n) du += bf16d(dY[r * h + n]) * br[n];
+                double dha = du * g * silu_grad(a), dhg = du * silu(a), u = silu(a) * g;
+                for (int64_t k = 0; k < h; ++k) {
+                    double xv = bf16d(X[r * h + k]);
+                    dAc[c * h + k] += xv * dha;
+                    dWc[c * h + k] += xv * dhg;
+                }
+                for (int64_t n = 0; n < h; ++n) dBc[c * h + n] += u * bf16d(dY[r * h + n]);
+            }
+        }
+        free(ac); free(wc); free(br);
+    }
+    return 0;
+}

@@ -83,3 +83,16 @@ def test_swiglu_gate_of_zero_blocks_everything():
     np.testing.assert_array_equal(out["Y"], 0.0)
     np.testing.assert_array_equal(out["dA"], 0.0)
     np.testing.assert_array_equal(out["dB"], 0.0)
+
+
+def test_swiglu_sampled_matches_full_on_bf16_inputs():
+    from megatron_tensor_transformer_tcgen05_gb300.inputs import make_swiglu_inputs
+    inp = make_swiglu_inputs(40, 24, 64, seed=3, sdy=1.0, sw=0.2)
+    full = oracle.swiglu_fwd_bwd(inp)
+    rows, cols = np.array([0, 9, 39]), np.array([0, 31, 32, 63])
+    s = oracle.swiglu_sampled_bf16(inp, rows, cols)
+    np.testing.assert_allclose(s["Y_rows"], full["Y"][rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s["dX_rows"], full["dX"][rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s["dA_cols"], full["dA"][:, cols], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s["dWg_cols"], full["dWg"][:, cols], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s["dB_rows"], full["dB"][cols], rtol=1e-12, atol=1e-12)
