@@ -75,6 +75,12 @@ def _load():
             lib.oracle_swiglu_backward.argtypes = [i64, i64, i64] + [dp] * 12
             lib.oracle_swiglu_sampled_bf16.restype = i32
             lib.oracle_swiglu_sampled_bf16.argtypes = [i64, i64, i64] + [dp] * 5 + [i64, dp, i64, dp] + [dp] * 5
+            lib.oracle_attn_forward.restype = i32
+            lib.oracle_attn_forward.argtypes = [i64] * 5 + [i32] + [dp] * 11
+            lib.oracle_attn_backward.restype = i32
+            lib.oracle_attn_backward.argtypes = [i64] * 5 + [dp] * 16
+            lib.oracle_attn_sharded.restype = i32
+            lib.oracle_attn_sharded.argtypes = [i64] * 6 + [i32] + [dp] * 14
             lib.oracle_swiglu_sharded.restype = i32
             lib.oracle_swiglu_sharded.argtypes = [i64, i64, i64, i64] + [dp] * 12
             _lib = lib
@@ -326,3 +332,50 @@ def swiglu_sampled_bf16(inp: dict, rows, cols) -> dict:
                                         _p(Yr), _p(dXr), _p(dAc), _p(dWc), _p(dBc))
     assert rc == 0, rc
     return {"Y_rows": Yr, "dX_rows": dXr, "dA_cols": dAc.T.copy(), "dWg_cols": dWc.T.copy(), "dB_rows": dBc}
+
+
+# ---- head-parallel self-attention block ---------------------------------------------------
+
+def attn_fwd_bwd(inp: dict, b: int, s: int, a: int, causal: bool = True) -> dict:
+    """Q, K, V, P, C, Y and dX, dWq, dWk, dWv, dWo of the attention block.
+
+    inp: X [b*s, h], Wq/Wk/Wv [h, a*d], Wo [a*d, h], dY [b*s, h]."""
+    lib = _load()
+    X, Wq, Wk, Wv, Wo, dY = (_f64(inp[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo", "dY"))
+    T, h = X.shape
+    hd = Wq.shape[1]
+    assert T == b * s and hd % a == 0
+    d = hd // a
+    o = {k: np.empty((T, hd)) for k in ("Q", "K", "V", "C")}
+    o["P"] = np.empty((b, a, s, s))
+    o["Y"] = np.empty((T, h))
+    rc = lib.oracle_attn_forward(b, s, h, a, d, int(causal), _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(o["Q"]),
+                                 _p(o["K"]), _p(o["V"]), _p(o["P"]), _p(o["C"]), _p(o["Y"]))
+    assert rc == 0, rc
+    o.update(dX=np.empty((T, h)), dWq=np.empty((h, hd)), dWk=np.empty((h, hd)), dWv=np.empty((h, hd)),
+             dWo=np.empty((hd, h)))
+    rc = lib.oracle_attn_backward(b, s, h, a, d, _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(o["Q"]), _p(o["K"]),
+                                  _p(o["V"]), _p(o["P"]), _p(o["C"]), _p(dY), _p(o["dX"]), _p(o["dWq"]),
+                                  _p(o["dWk"]), _p(o["dWv"]), _p(o["dWo"]))
+    assert rc == 0, rc
+    return o
+
+
+def attn_sharded(inp: dict, b: int, s: int, a: int, t: int, causal: bool = True, parts: bool = False) -> dict:
+    lib = _load()
+    X, Wq, Wk, Wv, Wo, dY = (_f64(inp[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo", "dY"))
+    T, h = X.shape
+    hd = Wq.shape[1]
+    d = hd // a
+    o = {"Y": np.empty((T, h)), "dX": np.empty((T, h)), "dWq": np.empty((h, hd)), "dWk": np.empty((h, hd)),
+         "dWv": np.empty((h, hd)), "dWo": np.empty((hd, h))}
+    Yp = np.empty((t, T, h)) if parts else None
+    dXp = np.empty((t, T, h)) if parts else None
+    rc = lib.oracle_attn_sharded(b, s, h, a, d, t, int(causal), _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(dY),
+                                 _p(o["Y"]), _p(o["dX"]), _p(o["dWq"]), _p(o["dWk"]), _p(o["dWv"]), _p(o["dWo"]),
+                                 _p(Yp) if parts else None, _p(dXp) if parts else None)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_sharded rejected a={a} t={t}")
+    if parts:
+        o["Y_part"], o["dX_part"] = Yp, dXp
+    return o

@@ -646,3 +646,183 @@ int oracle_swiglu_sampled_bf16(int64_t T, int64_t h, int64_t f, const uint16_t *
     }
     return 0;
 }
+
+/* ---- head-parallel self-attention block ---------------------------------------------- */
+
+/* "Efficient Large-Scale Language Model Training ... Megatron-LM", section 3, Figure 5b, and
+ * "Distributed training" (ml-interview-book), section 3.2 (tensor_parallel_attention): the
+ * heads are split across t shards (Wq, Wk, Wv by columns grouped by head, Wo by rows), each
+ * shard computes its heads' attention locally and the outputs of Wo sum over shards.
+ * Tokens are [b, s] (T = b*s rows, batch-major); each head sees only its own sequence.
+ *   Q = X Wq, K = X Wk, V = X Wv                               [T, hd]
+ *   S = Q_h K_h^T / sqrt(d) (+ causal mask: key > query -> -inf), P = softmax_rows(S)
+ *   C_h = P V_h, C = [C_1 | ... | C_a]                           [T, hd]
+ *   Y = C Wo                                                     [T, h]
+ * with a heads of width d (hd = a*d columns; the pages use hd = h). No biases. */
+static void attn_core_forward(int64_t b, int64_t s, int64_t a, int64_t d, int causal, const double *Q,
+                              const double *K, const double *V, double *P, double *C)
+{
+    const int64_t hd = a * d;
+    const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t bi = 0; bi < b; ++bi)
+        for (int64_t hh = 0; hh < a; ++hh) {
+            double *Pbh = P + (bi * a + hh) * s * s;
+            for (int64_t i = 0; i < s; ++i) {
+                const double *q = Q + (bi * s + i) * hd + hh * d;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < s; ++j) {
+                    double v = -INFINITY;
+                    if (!causal || j <= i) {
+                        const double *k = K + (bi * s + j) * hd + hh * d;
+                        double dot = 0.0;
+                        for (int64_t e = 0; e < d; ++e) dot += q[e] * k[e];
+                        v = dot * scale;
+                    }
+                    Pbh[i * s + j] = v;
+                    if (v > m) m = v;
+                }
+                double sum = 0.0;
+                for (int64_t j = 0; j < s; ++j) {
+                    double e = (Pbh[i * s + j] == -INFINITY) ? 0.0 : exp(Pbh[i * s + j] - m);
+                    Pbh[i * s + j] = e;
+                    sum += e;
+                }
+                for (int64_t j = 0; j < s; ++j) Pbh[i * s + j] /= sum;
+                double *c = C + (bi * s + i) * hd + hh * d;
+                for (int64_t e = 0; e < d; ++e) c[e] = 0.0;
+                for (int64_t j = 0; j < s; ++j) {
+                    const double p = Pbh[i * s + j];
+                    if (p == 0.0) continue;
+                    const double *v = V + (bi * s + j) * hd + hh * d;
+                    for (int64_t e = 0; e < d; ++e) c[e] += p * v[e];
+                }
+            }
+        }
+}
+
+int oracle_attn_forward(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, int causal, const double *X,
+                        const double *Wq, const double *Wk, const double *Wv, const double *Wo, double *Q,
+                        double *K, double *V, double *P, double *C, double *Y)
+{
+    if (b < 1 || s < 1 || h < 1 || a < 1 || d < 1) return 1;
+    const int64_t T = b * s, hd = a * d;
+    mm_nn(T, hd, h, X, Wq, Q);
+    mm_nn(T, hd, h, X, Wk, K);
+    mm_nn(T, hd, h, X, Wv, V);
+    attn_core_forward(b, s, a, d, causal, Q, K, V, P, C);
+    mm_nn(T, h, hd, C, Wo, Y);
+    return 0;
+}
+
+/* Backward given dY: dC = dY Wo^T; dWo = C^T dY; per head dV = P^T dC_h, dP = dC_h V_h^T,
+ * dS = P (.) (dP - rowsum(dP (.) P)), dQ_h = dS K_h / sqrt(d), dK_h = dS^T Q_h / sqrt(d);
+ * dX = dQ Wq^T + dK Wk^T + dV Wv^T; dWq = X^T dQ; dWk = X^T dK; dWv = X^T dV. */
+int oracle_attn_backward(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, const double *X,
+                         const double *Wq, const double *Wk, const double *Wv, const double *Wo, const double *Q,
+                         const double *K, const double *V, const double *P, const double *C, const double *dY,
+                         double *dX, double *dWq, double *dWk, double *dWv, double *dWo)
+{
+    if (b < 1 || s < 1 || h < 1 || a < 1 || d < 1) return 1;
+    const int64_t T = b * s, hd = a * d;
+    const double scale = 1.0 / sqrt((double)d);
+    double *dC = malloc(sizeof(double) * (size_t)(T * hd)), *dQ = calloc((size_t)(T * hd), sizeof(double));
+    double *dK = calloc((size_t)(T * hd), sizeof(double)), *dV = calloc((size_t)(T * hd), sizeof(double));
+    double *tmp = malloc(sizeof(double) * (size_t)(T * h));
+    if (!dC || !dQ || !dK || !dV || !tmp) return 2;
+    mm_nt(T, hd, h, dY, Wo, dC);
+    mm_tn(hd, h, T, C, dY, dWo);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t bi = 0; bi < b; ++bi)
+        for (int64_t hh = 0; hh < a; ++hh) {
+            const double *Pbh = P + (bi * a + hh) * s * s;
+            double *dS = malloc(sizeof(double) * (size_t)(s * s));
+            for (int64_t i = 0; i < s; ++i) {
+                const double *dc = dC + (bi * s + i) * hd + hh * d;
+                double rs = 0.0;
+                for (int64_t j = 0; j < s; ++j) {
+                    const double *v = V + (bi * s + j) * hd + hh * d;
+                    double dp = 0.0;
+                    for (int64_t e = 0; e < d; ++e) dp += dc[e] * v[e];
+                    dS[i * s + j] = dp;
+                    rs += dp * Pbh[i * s + j];
+                }
+                for (int64_t j = 0; j < s; ++j) dS[i * s + j] = Pbh[i * s + j] * (dS[i * s + j] - rs);
+            }
+            for (int64_t i = 0; i < s; ++i)
+                for (int64_t j = 0; j < s; ++j) {
+                    const double p = Pbh[i * s + j], g = dS[i * s + j] * scale;
+                    const double *dc = dC + (bi * s + i) * hd + hh * d;
+                    double *dv = dV + (bi * s + j) * hd + hh * d;
+                    double *dq = dQ + (bi * s + i) * hd + hh * d;
+                    double *dk = dK + (bi * s + j) * hd + hh * d;
+                    const double *k = K + (bi * s + j) * hd + hh * d;
+                    const double *q = Q + (bi * s + i) * hd + hh * d;
+                    for (int64_t e = 0; e < d; ++e) {
+                        dv[e] += p * dc[e];
+                        dq[e] += g * k[e];
+                        dk[e] += g * q[e];
+                    }
+                }
+            free(dS);
+        }
+    mm_nt(T, h, hd, dQ, Wq, dX);
+    mm_nt(T, h, hd, dK, Wk, tmp);
+    for (int64_t e = 0; e < T * h; ++e) dX[e] += tmp[e];
+    mm_nt(T, h, hd, dV, Wv, tmp);
+    for (int64_t e = 0; e < T * h; ++e) dX[e] += tmp[e];
+    mm_tn(h, hd, T, X, dQ, dWq);
+    mm_tn(h, hd, T, X, dK, dWk);
+    mm_tn(h, hd, T, X, dV, dWv);
+    free(dC); free(dQ); free(dK); free(dV); free(tmp);
+    return 0;
+}
+
+/* Shard by shard: shard i owns heads [i a/t, (i+1) a/t): its columns of Wq, Wk, Wv and its
+ * rows of Wo; Y = sum_i C_i Wo_i (the one sum), dX = sum_i dX_i. Y_part, dX_part (optional)
+ * receive the per-shard partials [t,T,h]. */
+int oracle_attn_sharded(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, int64_t t, int causal,
+                        const double *X, const double *Wq, const double *Wk, const double *Wv, const double *Wo,
+                        const double *dY, double *Y, double *dX, double *dWq, double *dWk, double *dWv,
+                        double *dWo, double *Y_part, double *dX_part)
+{
+    if (b < 1 || s < 1 || h < 1 || a < 1 || d < 1 || t < 1 || a % t != 0) return 1;
+    const int64_t T = b * s, hd = a * d, as = a / t, cs = as * d;
+    size_t nw = (size_t)(h * cs), nt = (size_t)(T * cs), nth = (size_t)(T * h);
+    double *q = malloc(sizeof(double) * nw), *k = malloc(sizeof(double) * nw), *v = malloc(sizeof(double) * nw);
+    double *o = malloc(sizeof(double) * nw), *Qi = malloc(sizeof(double) * nt), *Ki = malloc(sizeof(double) * nt);
+    double *Vi = malloc(sizeof(double) * nt), *Ci = malloc(sizeof(double) * nt);
+    double *Pi = malloc(sizeof(double) * (size_t)(b * as * s * s)), *Yi = malloc(sizeof(double) * nth);
+    double *dXi = malloc(sizeof(double) * nth), *gq = malloc(sizeof(double) * nw), *gk = malloc(sizeof(double) * nw);
+    double *gv = malloc(sizeof(double) * nw), *go = malloc(sizeof(double) * nw);
+    if (!q || !k || !v || !o || !Qi || !Ki || !Vi || !Ci || !Pi || !Yi || !dXi || !gq || !gk || !gv || !go) return 2;
+    for (int64_t e = 0; e < T * h; ++e) { Y[e] = 0.0; dX[e] = 0.0; }
+    for (int64_t sh = 0; sh < t; ++sh) {
+        const int64_t c0 = sh * cs;
+        for (int64_t r = 0; r < h; ++r)
+            for (int64_t c = 0; c < cs; ++c) {
+                q[r * cs + c] = Wq[r * hd + c0 + c];
+                k[r * cs + c] = Wk[r * hd + c0 + c];
+                v[r * cs + c] = Wv[r * hd + c0 + c];
+            }
+        for (int64_t c = 0; c < cs; ++c)
+            for (int64_t n = 0; n < h; ++n) o[c * h + n] = Wo[(c0 + c) * h + n];
+        oracle_attn_forward(b, s, h, as, d, causal, X, q, k, v, o, Qi, Ki, Vi, Pi, Ci, Yi);
+        for (int64_t e = 0; e < T * h; ++e) Y[e] += Yi[e];
+        if (Y_part) memcpy(Y_part + sh * T * h, Yi, sizeof(double) * nth);
+        oracle_attn_backward(b, s, h, as, d, X, q, k, v, o, Qi, Ki, Vi, Pi, Ci, dY, dXi, gq, gk, gv, go);
+        for (int64_t e = 0; e < T * h; ++e) dX[e] += dXi[e];
+        if (dX_part) memcpy(dX_part + sh * T * h, dXi, sizeof(double) * nth);
+        for (int64_t r = 0; r < h; ++r)
+            for (int64_t c = 0; c < cs; ++c) {
+                dWq[r * hd + c0 + c] = gq[r * cs + c];
+                dWk[r * hd + c0 + c] = gk[r * cs + c];
+                dWv[r * hd + c0 + c] = gv[r * cs + c];
+            }
+        for (int64_t c = 0; c < cs; ++c)
+            for (int64_t n = 0; n < h; ++n) dWo[(c0 + c) * h + n] = go[c * h + n];
+    }
+    free(q); free(k); free(v); free(o); free(Qi); free(Ki); free(Vi); free(Ci); free(Pi); free(Yi); free(dXi);
+    free(gq); free(gk); free(gv); free(go);
+    return 0;
+}
