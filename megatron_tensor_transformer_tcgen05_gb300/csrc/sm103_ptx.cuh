@@ -1,6 +1,6 @@
 // sm103_ptx.cuh -- hand-written inline-PTX wrappers for sm_103a: mbarrier with bounded
 // waits, TMA tile copies (cp.async.bulk.tensor), and the tcgen05 tensor-core / TMEM ops.
-// No TMA multicast is used. Every wait here is bounded: it gives up after a time
+// No multicast of any kind is used. Every wait here is bounded: it gives up after a time
 // limit, records an error code in a device status word and returns false, so a kernel
 // never spins forever.
 #pragma once
@@ -280,20 +280,20 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
-// Arrive once, on the mbarrier at the same offset in every CTA of `cta_mask`, when every
-// tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
+// Arrive once on the mbarrier at shared::cluster address `bar` (this CTA's or its peer's, as
+// given by mapa) when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Pair form: arrive on the barrier at offset `bar` in both CTAs of the pair (two unicast
+// commits: this CTA's own barrier, then the peer's through its mapa address).
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar)
+{
+    umma_commit_pair(bar);
+    umma_commit_pair(mapa_shared(bar, 1u));
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
@@ -318,6 +318,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr)
         : "memory");
 }
+
+// Warp-wide: thread i writes TMEM lane (lane base + i), 32 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     any = true;
                     // the stage is free, in both CTAs, once these MMAs finish
                     if (CG == 2)
-                        umma_commit_pair_mc(b_empty + 8u * stage, 0x3);
+                        umma_commit_pair_both(b_empty + 8u * stage);
                     else
                         umma_commit(b_empty + 8u * stage);
                     if (++stage == C::STAGES) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 if (!ok) break;
                 // accumulator ready for the epilogue warps of both CTAs
                 if (CG == 2)
-                    umma_commit_pair_mc(b_accf + 8u * acc, 0x3);
+                    umma_commit_pair_both(b_accf + 8u * acc);
                 else
                     umma_commit(b_accf + 8u * acc);
                 acc ^= 1u;
