@@ -51,7 +51,8 @@ extern "C" {
 typedef enum {
     MLP_OK = 0,
     MLP_EINVAL = 1,       /* NULL pointer, t < 1, T < 0, h or f < 8 */
-    MLP_ESHAPE = 2,       /* f % t != 0, or h, f, f/t not multiples of 8 */
+    MLP_ESHAPE = 2,       /* a size breaks the call's shape rules (MLP: f % t != 0, or h, f,
+                             f/t not multiples of 8; attention: a % t != 0, d != 128) */
     MLP_EALIGN = 3,       /* a pointer is not 16-byte aligned */
     MLP_ECUDA = 4,        /* a CUDA runtime call or launch failed */
     MLP_ETIMEOUT = 5,     /* a bounded device-side wait ran out (reported by query) */
@@ -193,11 +194,67 @@ enum {
     MLP_K_COLSUM_PARTIAL = 6,/* db partial column sums (da's come from the dH GEMM) */
     MLP_K_COLSUM_FINAL = 7,  /* da, db final sums */
     MLP_K_DROPOUT_BWD = 8,   /* dY = dZ (.) keep / (1 - p) */
-    MLP_NUM_KERNELS = 9
+    MLP_K_ATTN_QKV = 9,      /* attention: QKV = X*Wqkv */
+    MLP_K_ATTN_FWD = 10,     /* attention: C = softmax(mask(Q K^T / sqrt(d))) V per head, and L */
+    MLP_K_ATTN_OUT = 11,     /* attention: Y = C*Wo (sum over head shards) */
+    MLP_K_ATTN_DC = 12,      /* attention: dC = dY*Wo^T */
+    MLP_K_ATTN_DWO = 13,     /* attention: dWo = C^T*dY */
+    MLP_K_ATTN_DOT = 14,     /* attention: D = rowsum(dC (.) C) per head */
+    MLP_K_ATTN_DQ = 15,      /* attention: dQ */
+    MLP_K_ATTN_DKDV = 16,    /* attention: dK, dV */
+    MLP_K_ATTN_DX = 17,      /* attention: dX = dQKV*Wqkv^T (sum over Q, K, V and head shards) */
+    MLP_K_ATTN_DWQKV = 18,   /* attention: dWqkv = X^T*dQKV */
+    MLP_NUM_KERNELS = 19
 };
 mlp_status mlp_tp_timing_enable(int on);
 mlp_status mlp_tp_timing_collect(double* ms, int* counts);
 const char* mlp_tp_kernel_name(int kernel);
+
+/* ---- head-parallel self-attention block -----------------------------------------------
+ *
+ * The attention half of the Megatron layer ("Efficient Large-Scale Language Model Training
+ * on GPU Clusters Using Megatron-LM", section 3, Figure 5b; "Distributed training",
+ * ml-interview-book, section 2.6, and its section 3.2 head-parallel attention; "Parallelism",
+ * xuewyang.github.io, "Attention"): the query, key and value weights are split by columns
+ * grouped by head and the output weight by rows, so each of t shards owns a/t whole heads,
+ * runs their attention with no communication, and the shards' partial outputs are summed.
+ * Here all t shards live on one GPU and that sum is the K loop of the output projection's
+ * tensor-core accumulator. No biases (the pages' head-parallel attention has none).
+ *
+ *   QKV = X*Wqkv                       Wqkv = [Wq | Wk | Wv], each [h, a*d]
+ *   per head j:  S_j = Q_j K_j^T / sqrt(d)  (causal: key k > query q masked)
+ *                P_j = softmax over each row of S_j,   C_j = P_j V_j
+ *   C = [C_1 | ... | C_a]              Y = C*Wo,   Wo [a*d, h]
+ *
+ * Tokens are b sequences of s positions, batch-major: row bi*s + p of X is position p of
+ * sequence bi; attention never crosses sequences. Layout (row-major, dense):
+ *   X [T,h]  Wqkv [h,3*a*d]  Wo [a*d,h]  QKV [T,3*a*d]  C [T,a*d]  Y, dY, dX [T,h]
+ *   L [b*a, s] fp32: L[bi*a + j, p] = log2 sum_k 2^(S_j[p,k] * log2(e)), the base-2
+ *   log-sum-exp of position p's scaled scores in head j (kept for the backward pass).
+ *   Head j of Q (of K, V, C) is the column block [j*d, (j+1)*d) of its part; shard i owns
+ *   heads [i*a/t, (i+1)*a/t).
+ * Shapes: b >= 0, s >= 1, h >= 8 and h % 8 == 0, a >= 1, d == 128 (the one head width the
+ * kernels are written for; MLP_ESHAPE otherwise), t >= 1 with a % t == 0. Pointers as for
+ * the MLP block (token-indexed ones may be NULL when b == 0). Results are bitwise
+ * reproducible run to run (no atomics anywhere). */
+mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo, int b, int s, int h,
+                               int a, int d, int t, int causal, mlp_bf16* QKV, mlp_bf16* C, float* L, mlp_bf16* Y,
+                               void* cuda_stream);
+
+/* Device workspace mlp_tp_attn_backward needs (bytes; 0 for inadmissible shapes):
+ * dC [T, a*d] bf16 | D [b*a, s] fp32 | dQKV [T, 3*a*d] bf16, each 256-byte aligned. */
+size_t mlp_tp_attn_workspace_bytes(int b, int s, int h, int a, int d, int t);
+
+/* Backward of the attention block given dY and the forward's QKV, C and L:
+ *   dC = dY*Wo^T, dWo = C^T*dY, then per head (with D = rowsum(dC_j (.) C_j))
+ *   dP = dC_j V_j^T, dS = P (.) (dP - D), dQ_j = dS K_j / sqrt(d), dK_j = dS^T Q_j / sqrt(d),
+ *   dV_j = P^T dC_j, and dX = dQKV*Wqkv^T (the sum over Q, K, V and over head shards),
+ *   dWqkv = X^T*dQKV. dWqkv [h, 3*a*d] and dWo [a*d, h] are overwritten. The workspace
+ *   (256-byte aligned, at least mlp_tp_attn_workspace_bytes) holds dQKV on return. */
+mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo, const mlp_bf16* QKV,
+                                const mlp_bf16* C, const float* L, const mlp_bf16* dY, int b, int s, int h, int a,
+                                int d, int t, int causal, mlp_bf16* dX, mlp_bf16* dWqkv, mlp_bf16* dWo,
+                                void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 #ifdef __cplusplus
 }

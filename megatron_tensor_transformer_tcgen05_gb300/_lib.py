@@ -84,6 +84,12 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_swiglu_workspace_bytes.argtypes = [i32] * 4
             L.mlp_tp_bias_grads_noalloc.restype = i32
             L.mlp_tp_bias_grads_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+            L.mlp_tp_attn_forward.restype = i32
+            L.mlp_tp_attn_forward.argtypes = [vp] * 3 + [i32] * 7 + [vp] * 4 + [vp]
+            L.mlp_tp_attn_workspace_bytes.restype = sz
+            L.mlp_tp_attn_workspace_bytes.argtypes = [i32] * 6
+            L.mlp_tp_attn_backward.restype = i32
+            L.mlp_tp_attn_backward.argtypes = [vp] * 7 + [i32] * 7 + [vp] * 4 + [sz, vp]
             _lib = L
     return _lib
 
@@ -156,7 +162,7 @@ def mlp_tp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
            "mlp_tp_selftest_wait_timeout")
 
 
-MLP_NUM_KERNELS = 9
+MLP_NUM_KERNELS = 19
 
 
 def mlp_tp_timing_enable(on: bool) -> None:
@@ -207,3 +213,20 @@ def mlp_tp_swiglu_backward(X, A, Wg, B, Ha, Hg, U, dY, T: int, h: int, f: int, t
 
 def mlp_tp_swiglu_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
     return int(lib().mlp_tp_swiglu_workspace_bytes(T, h, f, t))
+
+
+def mlp_tp_attn_forward(X, Wqkv, Wo, b: int, s: int, h: int, a: int, d: int, t: int, causal: bool, QKV, C, L, Y,
+                        stream=None) -> None:
+    _check(lib().mlp_tp_attn_forward(_ptr(X), _ptr(Wqkv), _ptr(Wo), b, s, h, a, d, t, int(bool(causal)), _ptr(QKV),
+                                     _ptr(C), _ptr(L), _ptr(Y), _stream(stream)), "mlp_tp_attn_forward")
+
+
+def mlp_tp_attn_workspace_bytes(b: int, s: int, h: int, a: int, d: int, t: int) -> int:
+    return int(lib().mlp_tp_attn_workspace_bytes(b, s, h, a, d, t))
+
+
+def mlp_tp_attn_backward(X, Wqkv, Wo, QKV, C, L, dY, b: int, s: int, h: int, a: int, d: int, t: int, causal: bool,
+                         dX, dWqkv, dWo, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib().mlp_tp_attn_backward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(QKV), _ptr(C), _ptr(L), _ptr(dY), b, s, h,
+                                      a, d, t, int(bool(causal)), _ptr(dX), _ptr(dWqkv), _ptr(dWo), _ptr(workspace),
+                                      workspace_bytes, _stream(stream)), "mlp_tp_attn_backward")

@@ -75,3 +75,43 @@ def swiglu_step(inp: dict, buf: dict, t: int, stream=None) -> None:
                           buf["Y"], stream)
     mlp_tp_swiglu_backward(inp["X"], inp["A"], inp["Wg"], inp["B"], buf["Ha"], buf["Hg"], buf["U"], inp["dY"], T, h,
                            f, t, buf["dX"], buf["dA"], buf["dWg"], buf["dB"], buf["ws"], buf["ws"].numel(), stream)
+
+
+# ---- head-parallel attention block ----------------------------------------------------------
+
+def empty_attn_buffers(b: int, s: int, h: int, a: int, d: int, t: int, device="cuda") -> dict[str, torch.Tensor]:
+    from ._lib import mlp_tp_attn_workspace_bytes
+    bf = torch.bfloat16
+    ws = mlp_tp_attn_workspace_bytes(b, s, h, a, d, t)
+    if ws == 0 and b > 0:
+        raise ValueError(f"invalid sizes b={b} s={s} h={h} a={a} d={d} t={t}")
+    ws = max(ws, 256)
+    T, hd = b * s, a * d
+    return {"QKV": torch.empty((T, 3 * hd), dtype=bf, device=device), "C": torch.empty((T, hd), dtype=bf, device=device),
+            "L": torch.empty((b * a, s), dtype=torch.float32, device=device),
+            "Y": torch.empty((T, h), dtype=bf, device=device), "dX": torch.empty((T, h), dtype=bf, device=device),
+            "dWqkv": torch.empty((h, 3 * hd), dtype=bf, device=device),
+            "dWo": torch.empty((hd, h), dtype=bf, device=device),
+            "ws": torch.empty((ws,), dtype=torch.uint8, device=device)}
+
+
+def attn_forward(inp: dict, buf: dict, b: int, s: int, a: int, t: int, causal: bool = True, stream=None) -> None:
+    from ._lib import mlp_tp_attn_forward
+    h = inp["X"].shape[1]
+    d = inp["Wqkv"].shape[1] // (3 * a)
+    mlp_tp_attn_forward(inp["X"], inp["Wqkv"], inp["Wo"], b, s, h, a, d, t, causal, buf["QKV"], buf["C"], buf["L"],
+                        buf["Y"], stream)
+
+
+def attn_backward(inp: dict, buf: dict, b: int, s: int, a: int, t: int, causal: bool = True, stream=None) -> None:
+    from ._lib import mlp_tp_attn_backward
+    h = inp["X"].shape[1]
+    d = inp["Wqkv"].shape[1] // (3 * a)
+    mlp_tp_attn_backward(inp["X"], inp["Wqkv"], inp["Wo"], buf["QKV"], buf["C"], buf["L"], inp["dY"], b, s, h, a, d,
+                         t, causal, buf["dX"], buf["dWqkv"], buf["dWo"], buf["ws"], buf["ws"].numel(), stream)
+
+
+def attn_step(inp: dict, buf: dict, b: int, s: int, a: int, t: int, causal: bool = True, stream=None) -> None:
+    """One forward + backward of the attention block."""
+    attn_forward(inp, buf, b, s, a, t, causal, stream)
+    attn_backward(inp, buf, b, s, a, t, causal, stream)

@@ -1,0 +1,932 @@
+// attention.cu -- fused causal self-attention for the head-parallel attention block, on
+// tcgen05 tensor cores with TMEM accumulators, for sm_103a.
+//
+// Per head h of width d = 128, with Q, K, V the head's columns of the QKV projection:
+//   S = Q K^T / sqrt(d),  key j > query i masked when causal,  P = softmax_rows(S),  C = P V
+// ("Efficient Large-Scale Language Model Training on GPU Clusters Using Megatron-LM",
+// section 3, Figure 5b: each tensor-parallel shard runs whole heads, so the softmax never
+// crosses a shard; the pages fuse scale, mask and softmax into one kernel with the causal
+// mask implicit, section 4 "kernel fusion"). Here the whole of S -> P -> C also stays on
+// chip: S is never written to HBM.
+//
+// Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 192 threads.
+//   warp 0     TMA: the Q block once, then K and V blocks of 128 keys into a 2-stage ring
+//   warp 1     TMEM allocation and every tcgen05.mma: S_j = Q K_j^T into one of two TMEM
+//              S buffers, O += P_j V_j into the TMEM output accumulator
+//   warps 2-5  softmax, thread r <-> query row r (TMEM lane r): read S_j from TMEM, mask,
+//              running row max and sum (base 2), P_j -> shared memory (bf16, the A operand
+//              of the next MMA); rescale O in TMEM only when the row max has grown by more
+//              than 2^8 since the last rescale (the final division by the row sum makes the
+//              result exact whatever reference the exponentials used). Finally C = O / l and
+//              the row's base-2 log-sum-exp L for the backward pass.
+// Backward, deterministic (no atomics), two kernels that each recompute P from Q, K and L:
+//   attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key block), looping over 64-query
+//     blocks: S^T = K Q^T, dP^T = V dC^T, P^T = exp2(S^T c - L), dS^T = P^T (dP^T - D),
+//     dV += P^T dC, dK += dS^T Q.
+//   attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query block), looping over 64-key
+//     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D), dQ += dS K.
+//   with D = rowsum(dC * C) from attn_bwd_dot_kernel.
+// A tile of Q, K, V or dC is loaded once, row-major with a 128-byte swizzle, and read by
+// the tensor core both as a K-major operand (contraction over d) and as an MN-major one
+// (contraction over tokens): only the shared-memory descriptor differs, nothing is
+// transposed in memory.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "attn_args.h"
+#include "sm103_ptx.cuh"
+
+namespace mlp {
+
+namespace {
+
+constexpr unsigned long long kAttnDrainNs = 2000000000ull;
+constexpr int kLazyRescaleLog2 = 8;  // rescale O once the row max grows by more than 2^8
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// 2^x on the special-function unit (hand-written wrapper of the PTX instruction;
+// ex2 of -inf is +0, which is what a masked score needs).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Row r of a K-major, 128-byte-swizzled bf16 operand tile with ROWS rows: columns
+// [64k, 64k+64) form chunk k (ROWS x 128 bytes); 16-byte unit u of a row sits at unit
+// u ^ (r % 8), the layout a TMA SWIZZLE_128B load produces and the descriptors expect.
+template <int NCOLS, int ROWS>
+__device__ __forceinline__ void store_row_sw128(uint32_t buf, int r, const float (&v)[NCOLS])
+{
+#pragma unroll
+    for (int kc = 0; kc < NCOLS / 64; ++kc)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = 64 * kc + 8 * u;
+            sts128(buf + static_cast<uint32_t>(kc * ROWS * 128 + r * 128) + ((static_cast<uint32_t>(u) ^ (r & 7)) << 4),
+                   pack2_bf16(v[c], v[c + 1]), pack2_bf16(v[c + 2], v[c + 3]), pack2_bf16(v[c + 4], v[c + 5]),
+                   pack2_bf16(v[c + 6], v[c + 7]));
+        }
+}
+
+// 32 fp32 values * mul -> 32 bf16 at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store32_global(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul)
+{
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 w;
+        w.x = pack2_bf16(__uint_as_float(r[8 * i + 0]) * mul, __uint_as_float(r[8 * i + 1]) * mul);
+        w.y = pack2_bf16(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul);
+        w.z = pack2_bf16(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul);
+        w.w = pack2_bf16(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul);
+        d4[i] = w;
+    }
+}
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc_sw128(addr, 16u, 1024u); }
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t chunk_stride)
+{
+    return smem_desc_sw128(addr, chunk_stride, 1024u);
+}
+
+// One lane waits; the warp follows its verdict (TMEM loads are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          unsigned long long limit, int code, int wa, int wb)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, status, limit, code, wa, wb);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Producer-side drain after an abort: wait (bounded, ignoring the abort flag) for every
+// copy this CTA started, so that none lands after the CTA has exited.
+__device__ __forceinline__ void drain_loads(uint32_t bars, int nbars, uint32_t issued, uint32_t par, int* status)
+{
+    volatile int never = 0;
+    for (int i = 0; i < nbars; ++i)
+        if (issued & (1u << i))
+            mbar_wait_bounded(bars + 8u * i, (par >> i) & 1u, &never, status, kAttnDrainNs, DEV_TIMEOUT_DRAIN);
+}
+
+__device__ __forceinline__ void drain_mma(uint32_t bar, int* status)
+{
+    volatile int never = 0;
+    umma_commit(bar);
+    mbar_wait_bounded(bar, 0, &never, status, kAttnDrainNs, DEV_TIMEOUT_DRAIN);
+}
+
+// ---- forward -------------------------------------------------------------------------------
+
+struct FwdCfg {
+    static constexpr int BQ = 128, BKV = 128;
+    static constexpr uint32_t TILE = 128 * kHeadDim * 2;  // a 128 x 128 bf16 tile: 32 KB
+    static constexpr uint32_t OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE, OFF_BAR = 7 * TILE;
+    // barriers: q | kfull[2] | vfull[2] | kvempty[2] | sfull[2] | sfree[2] | pfull[2] | pvdone[2] | drain
+    static constexpr int NUM_BARS = 16;
+    static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);
+    static constexpr uint32_t TMEM_COLS = 512;  // S[0] 0..127 | S[1] 128..255 | O 256..383
+    static constexpr uint32_t O_COL = 256;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args)
+{
+    using C = FwdCfg;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V, sP = base + C::OFF_P;
+    const uint32_t bar = base + C::OFF_BAR;
+    const uint32_t b_q = bar, b_kf = bar + 8, b_vf = bar + 24, b_kve = bar + 40, b_sf = bar + 56, b_sfree = bar + 72,
+                   b_pf = bar + 88, b_pv = bar + 104, b_drain = bar + 120;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = args.s, a = args.a;
+    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
+    const int qb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest rows first
+    const int q0 = qb * C::BQ;
+    const int nkb_all = (s + C::BKV - 1) / C::BKV;
+    const int nkb = args.causal ? min(nkb_all, qb + 1) : nkb_all;
+    const int row0 = bi * s;
+    const int hd = a * kHeadDim;
+    const int colQ = head * kHeadDim, colK = hd + colQ, colV = 2 * hd + colQ;
+    const unsigned long long limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_kf + 8 * i, 1);
+            mbar_init(b_vf + 8 * i, 1);
+            mbar_init(b_kve + 8 * i, 1);
+            mbar_init(b_sf + 8 * i, 1);
+            mbar_init(b_sfree + 8 * i, 4);
+            mbar_init(b_pf + 8 * i, 4);
+            mbar_init(b_pv + 8 * i, 1);
+        }
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&args.tmQ);
+        tma_prefetch_desc(&args.tmKV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            // barrier index for the drain: 0 = q, 1..2 = kfull, 3..4 = vfull
+            uint32_t issued = 1u, par = 0u;
+            bool ok = true;
+            mbar_arrive_expect_tx(b_q, 2 * C::TILE / 2);
+            tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_q);
+            tma_load_2d(sQ + C::TILE / 2, &args.tmQ, colQ + 64, row0 + q0, b_q);
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait_bounded(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                                 DEV_TIMEOUT_PRODUCER, 1000, j)) {
+                    ok = false;
+                    break;
+                }
+                const int y = row0 + j * C::BKV;
+                const uint32_t ph = (j >> 1) & 1;
+                mbar_arrive_expect_tx(b_kf + 8 * st, C::TILE);
+                tma_load_2d(sK + st * C::TILE, &args.tmKV, colK, y, b_kf + 8 * st);
+                tma_load_2d(sK + st * C::TILE + C::TILE / 2, &args.tmKV, colK + 64, y, b_kf + 8 * st);
+                mbar_arrive_expect_tx(b_vf + 8 * st, C::TILE);
+                tma_load_2d(sV + st * C::TILE, &args.tmKV, colV, y, b_vf + 8 * st);
+                tma_load_2d(sV + st * C::TILE + C::TILE / 2, &args.tmKV, colV + 64, y, b_vf + 8 * st);
+                issued |= (1u << (1 + st)) | (1u << (3 + st));
+                par = (par & ~((1u << (1 + st)) | (1u << (3 + st)))) | (ph << (1 + st)) | (ph << (3 + st));
+            }
+            if (!ok) drain_loads(bar, 5, issued, par, args.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(b_q, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 1001, -1);
+            bool any = false;
+            for (int j = 0; ok && j <= nkb; ++j) {
+                if (j < nkb) {
+                    const int st = j & 1;
+                    if (!mbar_wait_bounded(b_kf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL, 1002, j) ||
+                        (j >= 2 && !mbar_wait_bounded(b_sfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
+                                                      limit, DEV_TIMEOUT_MMA_ACC, 1003, j))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbuf = sK + st * C::TILE;
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t off = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
+                        umma_bf16(tmem + 128u * st, desc_k(sQ + off), desc_k(kbuf + off), C::IDESC_S, k > 0);
+                    }
+                    any = true;
+                    umma_commit(b_sf + 8 * st);
+                }
+                if (j >= 1) {
+                    const int pj = j - 1, pst = pj & 1;
+                    if (!mbar_wait_bounded(b_pf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_ACC, 1004, pj) ||
+                        !mbar_wait_bounded(b_vf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL, 1005, pj)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pbuf = sP + pst * C::TILE, vbuf = sV + pst * C::TILE;
+#pragma unroll
+                    for (int k = 0; k < C::BKV / 16; ++k) {
+                        const uint32_t aoff = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
+                        umma_bf16(tmem + C::O_COL, desc_k(pbuf + aoff), desc_mn(vbuf + 2048u * k, C::TILE / 2),
+                                  C::IDESC_PV, (pj > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(b_pv + 8 * pst);
+                    umma_commit(b_kve + 8 * pst);
+                }
+            }
+            if (!ok && any) drain_mma(b_drain, args.status);
+        }
+    } else {
+        // ------------------------------ softmax -----------------------------------
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const int qi = q0 + r;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        float m_used = NEG_INF, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkb; ++j) {
+            const int st = j & 1;
+            if (!warp_wait(b_sf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1006, j)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[C::BKV];
+            {
+                uint32_t u[32];
+#pragma unroll
+                for (int c = 0; c < C::BKV / 32; ++c) {
+                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(u[i]) * args.scale_log2;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_sfree + 8 * st);
+            const int k0 = j * C::BKV;
+            if ((args.causal && k0 + C::BKV - 1 > q0) || k0 + C::BKV > s) {  // CTA-uniform
+#pragma unroll
+                for (int c = 0; c < C::BKV; ++c) {
+                    const int key = k0 + c;
+                    if (key >= s || (args.causal && key > qi)) x[c] = NEG_INF;
+                }
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < C::BKV; ++c) mx = fmaxf(mx, x[c]);
+            const bool resc = mx > m_used + static_cast<float>(kLazyRescaleLog2);
+            float alpha = 1.0f;
+            if (resc) {
+                alpha = ex2(m_used - mx);  // 0 when m_used is -inf
+                m_used = mx;
+                l *= alpha;
+            }
+            const float mref = (m_used == NEG_INF) ? 0.0f : m_used;
+            float rs = 0.0f;
+#pragma unroll
+            for (int c = 0; c < C::BKV; ++c) {
+                x[c] = ex2(x[c] - mref);
+                rs += x[c];
+            }
+            l += rs;
+            // the P buffer is free once PV_{j-2} has completed
+            if (j >= 2 && !warp_wait(b_pv + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                     DEV_TIMEOUT_EPILOGUE, 1007, j)) {
+                ok = false;
+                break;
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+                // O holds PV_0..PV_{j-1} once PV_{j-1} has completed: rescale it in place
+                if (!warp_wait(b_pv + 8 * (st ^ 1), ((j - 1) >> 1) & 1, abort_flag, args.status, limit,
+                               DEV_TIMEOUT_EPILOGUE, 1008, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t o[32];
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    tmem_ld_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
+                }
+                tmem_st_wait();
+            }
+            store_row_sw128<C::BKV, C::BQ>(sP + st * C::TILE, r, x);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pf + 8 * st);
+        }
+        if (ok && nkb > 0 &&
+            warp_wait(b_pv + 8 * ((nkb - 1) & 1), ((nkb - 1) >> 1) & 1, abort_flag, args.status, limit,
+                      DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
+            tc_fence_after();
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ;
+            uint32_t o[32];
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
+                tmem_ld_wait();
+                if (qi < s) store32_global(dst + 32 * c, o, inv_l);
+            }
+            if (qi < s) args.lse[static_cast<size_t>(bh) * s + qi] = m_used + log2f(l);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---- backward: dK and dV ---------------------------------------------------------------------
+
+struct DkdvCfg {
+    static constexpr int BKV = 128, BQ = 64;
+    static constexpr uint32_t KT = 128 * kHeadDim * 2;  // K or V block: 32 KB
+    static constexpr uint32_t QT = 64 * kHeadDim * 2;   // Q or dC block: 16 KB
+    static constexpr uint32_t PT = 128 * 64 * 2;        // P^T or dS^T block: 16 KB
+    static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_Q = 2 * KT, OFF_DO = 2 * KT + 2 * QT,
+                              OFF_P = 2 * KT + 4 * QT, OFF_DS = OFF_P + 2 * PT, OFF_LD = OFF_DS + 2 * PT,
+                              OFF_BAR = OFF_LD + 4 * 2 * 64 * 4;
+    // barriers: kv | qdofull[2] | qdoempty[2] | stfull[2] | stfree[2] | pdfull[2] | accfull | drain
+    static constexpr int NUM_BARS = 13;
+    static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
+    static constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
+    static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, 128, false, true);
+    static constexpr uint32_t TMEM_COLS = 512;  // S^T[x] at 128x, dP^T[x] at 128x + 64; dV 256; dK 384
+    static constexpr uint32_t DV_COL = 256, DK_COL = 384;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnArgs args)
+{
+    using C = DkdvCfg;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q, sdO = base + C::OFF_DO,
+                   sP = base + C::OFF_P, sdS = base + C::OFF_DS, sLD = base + C::OFF_LD;
+    const uint32_t bar = base + C::OFF_BAR;
+    const uint32_t b_kv = bar, b_qf = bar + 8, b_qe = bar + 24, b_stf = bar + 40, b_stfree = bar + 56,
+                   b_pdf = bar + 72, b_acc = bar + 88, b_drain = bar + 96;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = args.s, a = args.a;
+    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
+    const int kb = static_cast<int>(blockIdx.y);  // with a causal mask, low key blocks have the most queries
+    const int k0 = kb * C::BKV;
+    const int nqb_all = (s + C::BQ - 1) / C::BQ;
+    const int qb_first = args.causal ? k0 / C::BQ : 0;
+    const int nq = nqb_all - qb_first;
+    const int row0 = bi * s;
+    const int hd = a * kHeadDim;
+    const int colQ = head * kHeadDim, colK = hd + colQ, colV = 2 * hd + colQ;
+    const unsigned long long limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_qf + 8 * i, 1);
+            mbar_init(b_qe + 8 * i, 1);
+            mbar_init(b_stf + 8 * i, 1);
+            mbar_init(b_stfree + 8 * i, 4);
+            mbar_init(b_pdf + 8 * i, 4);
+        }
+        mbar_init(b_acc, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&args.tmQ);
+        tma_prefetch_desc(&args.tmKV);
+        tma_prefetch_desc(&args.tmdO);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // drain indices: 0 = kv, 1..2 = qdofull
+            uint32_t issued = 1u, par = 0u;
+            bool ok = true;
+            mbar_arrive_expect_tx(b_kv, 2 * C::KT);
+            tma_load_2d(sK, &args.tmKV, colK, row0 + k0, b_kv);
+            tma_load_2d(sK + C::KT / 2, &args.tmKV, colK + 64, row0 + k0, b_kv);
+            tma_load_2d(sV, &args.tmKV, colV, row0 + k0, b_kv);
+            tma_load_2d(sV + C::KT / 2, &args.tmKV, colV + 64, row0 + k0, b_kv);
+            for (int i = 0; i < nq; ++i) {
+                const int st = i & 1;
+                if (i >= 2 && !mbar_wait_bounded(b_qe + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                                 DEV_TIMEOUT_PRODUCER, 3000, i)) {
+                    ok = false;
+                    break;
+                }
+                const int y = row0 + (qb_first + i) * C::BQ;
+                mbar_arrive_expect_tx(b_qf + 8 * st, 2 * C::QT);
+                tma_load_2d(sQ + st * C::QT, &args.tmQ, colQ, y, b_qf + 8 * st);
+                tma_load_2d(sQ + st * C::QT + C::QT / 2, &args.tmQ, colQ + 64, y, b_qf + 8 * st);
+                tma_load_2d(sdO + st * C::QT, &args.tmdO, colQ, y, b_qf + 8 * st);
+                tma_load_2d(sdO + st * C::QT + C::QT / 2, &args.tmdO, colQ + 64, y, b_qf + 8 * st);
+                issued |= 1u << (1 + st);
+                par = (par & ~(1u << (1 + st))) | (static_cast<uint32_t>((i >> 1) & 1) << (1 + st));
+            }
+            if (!ok) drain_loads(bar, 3, issued, par, args.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(b_kv, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 3001, -1);
+            bool any = false;
+            for (int i = 0; ok && i <= nq; ++i) {
+                if (i < nq) {
+                    const int st = i & 1;
+                    if (!mbar_wait_bounded(b_qf + 8 * st, (i >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL, 3002, i) ||
+                        (i >= 2 && !mbar_wait_bounded(b_stfree + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status,
+                                                      limit, DEV_TIMEOUT_MMA_ACC, 3003, i))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qbuf = sQ + st * C::QT, dobuf = sdO + st * C::QT;
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t ka = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
+                        const uint32_t kq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
+                        umma_bf16(tmem + 128u * st, desc_k(sK + ka), desc_k(qbuf + kq), C::IDESC_ST, k > 0);
+                        umma_bf16(tmem + 128u * st + 64u, desc_k(sV + ka), desc_k(dobuf + kq), C::IDESC_ST, k > 0);
+                    }
+                    any = true;
+                    umma_commit(b_stf + 8 * st);
+                }
+                if (i >= 1) {
+                    const int pi = i - 1, pst = pi & 1;
+                    if (!mbar_wait_bounded(b_pdf + 8 * pst, (pi >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_ACC, 3004, pi)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qbuf = sQ + pst * C::QT, dobuf = sdO + pst * C::QT;
+                    const uint32_t pbuf = sP + pst * C::PT, dsbuf = sdS + pst * C::PT;
+#pragma unroll
+                    for (int k = 0; k < C::BQ / 16; ++k) {
+                        const uint32_t acc = (pi > 0 || k > 0) ? 1u : 0u;
+                        umma_bf16(tmem + C::DV_COL, desc_k(pbuf + 32u * k), desc_mn(dobuf + 2048u * k, C::QT / 2),
+                                  C::IDESC_ACC, acc);
+                        umma_bf16(tmem + C::DK_COL, desc_k(dsbuf + 32u * k), desc_mn(qbuf + 2048u * k, C::QT / 2),
+                                  C::IDESC_ACC, acc);
+                    }
+                    umma_commit(b_qe + 8 * pst);
+                }
+            }
+            if (ok && any) umma_commit(b_acc);
+            if (!ok && any) drain_mma(b_drain, args.status);
+        }
+    } else {
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const int kj = k0 + r;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t sL = sLD + static_cast<uint32_t>(q) * 512u, sD = sL + 256u;
+        const size_t lbase = static_cast<size_t>(bh) * s;
+        bool ok = true;
+        for (int i = 0; i < nq; ++i) {
+            const int st = i & 1;
+            const int qq0 = (qb_first + i) * C::BQ;
+            // this block's L and D into the warp's own staging slots
+            {
+                const int qa = qq0 + lane, qb2 = qq0 + 32 + lane;
+                const float la = qa < s ? args.lse[lbase + qa] : 0.0f, lb = qb2 < s ? args.lse[lbase + qb2] : 0.0f;
+                const float da = qa < s ? args.delta[lbase + qa] : 0.0f, db = qb2 < s ? args.delta[lbase + qb2] : 0.0f;
+                __syncwarp();
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sL + 4u * lane), "f"(la) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sL + 128u + 4u * lane), "f"(lb) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sD + 4u * lane), "f"(da) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sD + 128u + 4u * lane), "f"(db) : "memory");
+                __syncwarp();
+            }
+            if (!warp_wait(b_stf + 8 * st, (i >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3005, i)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float p[C::BQ], dp[C::BQ];
+            {
+                uint32_t u[32];
+#pragma unroll
+                for (int c = 0; c < C::BQ / 32; ++c) {
+                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) p[32 * c + e] = __uint_as_float(u[e]);
+                    tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + 32u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dp[32 * c + e] = __uint_as_float(u[e]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_stfree + 8 * st);
+            const bool need_mask = (args.causal && qq0 < k0 + C::BKV - 1) || qq0 + C::BQ > s || k0 + C::BKV > s;
+#pragma unroll
+            for (int c4 = 0; c4 < C::BQ / 4; ++c4) {
+                const float4 L4 = lds128f(sL + 16u * c4), D4 = lds128f(sD + 16u * c4);
+                const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * c4 + e;
+                    float pv = ex2(fmaf(p[c], args.scale_log2, -Lv[e]));
+                    if (need_mask) {
+                        const int qi = qq0 + c;
+                        if (qi >= s || kj >= s || (args.causal && kj > qi)) pv = 0.0f;
+                    }
+                    p[c] = pv;
+                    dp[c] = pv * (dp[c] - Dv[e]);
+                }
+            }
+            // P^T and dS^T buffers are free once the dV / dK MMAs of block i-2 completed
+            if (i >= 2 && !warp_wait(b_qe + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                     DEV_TIMEOUT_EPILOGUE, 3006, i)) {
+                ok = false;
+                break;
+            }
+            store_row_sw128<C::BQ, C::BKV>(sP + st * C::PT, r, p);
+            store_row_sw128<C::BQ, C::BKV>(sdS + st * C::PT, r, dp);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pdf + 8 * st);
+        }
+        if (ok && nq > 0 && warp_wait(b_acc, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3007, -1)) {
+            tc_fence_after();
+            __nv_bfloat16* rowp = args.out + static_cast<size_t>(row0 + kj) * (3 * hd);
+            uint32_t o[32];
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::DV_COL + 32u * c, o);
+                tmem_ld_wait();
+                if (kj < s) store32_global(rowp + colV + 32 * c, o, 1.0f);
+                tmem_ld_32x32b_x32(t_lane + C::DK_COL + 32u * c, o);
+                tmem_ld_wait();
+                if (kj < s) store32_global(rowp + colK + 32 * c, o, args.scale);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---- backward: dQ ----------------------------------------------------------------------------
+
+struct DqCfg {
+    static constexpr int BQ = 128, BKV = 64;
+    static constexpr uint32_t QT = 128 * kHeadDim * 2;  // Q or dC block: 32 KB
+    static constexpr uint32_t KT = 64 * kHeadDim * 2;   // K or V block: 16 KB
+    static constexpr uint32_t ST = 128 * 64 * 2;        // dS block: 16 KB
+    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_K = 2 * QT, OFF_V = 2 * QT + 2 * KT,
+                              OFF_DS = 2 * QT + 4 * KT, OFF_BAR = OFF_DS + 2 * ST;
+    // barriers: qdo | kvfull[2] | kvempty[2] | spfull[2] | spfree[2] | dsfull[2] | dqfull | drain
+    static constexpr int NUM_BARS = 13;
+    static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
+    static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 128, false, true);
+    static constexpr uint32_t TMEM_COLS = 512;  // S[x] at 128x, dP[x] at 128x + 64; dQ at 256
+    static constexpr uint32_t DQ_COL = 256;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnArgs args)
+{
+    using C = DqCfg;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sK = base + C::OFF_K, sV = base + C::OFF_V,
+                   sdS = base + C::OFF_DS;
+    const uint32_t bar = base + C::OFF_BAR;
+    const uint32_t b_qdo = bar, b_kvf = bar + 8, b_kve = bar + 24, b_spf = bar + 40, b_spfree = bar + 56,
+                   b_dsf = bar + 72, b_dq = bar + 88, b_drain = bar + 96;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = args.s, a = args.a;
+    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
+    const int qb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest rows first
+    const int q0 = qb * C::BQ;
+    const int nkb_all = (s + C::BKV - 1) / C::BKV;
+    const int nkb = args.causal ? min(nkb_all, (q0 + C::BQ - 1) / C::BKV + 1) : nkb_all;
+    const int row0 = bi * s;
+    const int hd = a * kHeadDim;
+    const int colQ = head * kHeadDim, colK = hd + colQ, colV = 2 * hd + colQ;
+    const unsigned long long limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_qdo, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_kvf + 8 * i, 1);
+            mbar_init(b_kve + 8 * i, 1);
+            mbar_init(b_spf + 8 * i, 1);
+            mbar_init(b_spfree + 8 * i, 4);
+            mbar_init(b_dsf + 8 * i, 4);
+        }
+        mbar_init(b_dq, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&args.tmQ);
+        tma_prefetch_desc(&args.tmKV);
+        tma_prefetch_desc(&args.tmdO);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t issued = 1u, par = 0u;  // drain indices: 0 = qdo, 1..2 = kvfull
+            bool ok = true;
+            mbar_arrive_expect_tx(b_qdo, 2 * C::QT);
+            tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_qdo);
+            tma_load_2d(sQ + C::QT / 2, &args.tmQ, colQ + 64, row0 + q0, b_qdo);
+            tma_load_2d(sdO, &args.tmdO, colQ, row0 + q0, b_qdo);
+            tma_load_2d(sdO + C::QT / 2, &args.tmdO, colQ + 64, row0 + q0, b_qdo);
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait_bounded(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                                 DEV_TIMEOUT_PRODUCER, 2000, j)) {
+                    ok = false;
+                    break;
+                }
+                const int y = row0 + j * C::BKV;
+                mbar_arrive_expect_tx(b_kvf + 8 * st, 2 * C::KT);
+                tma_load_2d(sK + st * C::KT, &args.tmKV, colK, y, b_kvf + 8 * st);
+                tma_load_2d(sK + st * C::KT + C::KT / 2, &args.tmKV, colK + 64, y, b_kvf + 8 * st);
+                tma_load_2d(sV + st * C::KT, &args.tmKV, colV, y, b_kvf + 8 * st);
+                tma_load_2d(sV + st * C::KT + C::KT / 2, &args.tmKV, colV + 64, y, b_kvf + 8 * st);
+                issued |= 1u << (1 + st);
+                par = (par & ~(1u << (1 + st))) | (static_cast<uint32_t>((j >> 1) & 1) << (1 + st));
+            }
+            if (!ok) drain_loads(bar, 3, issued, par, args.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(b_qdo, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 2001, -1);
+            bool any = false;
+            for (int j = 0; ok && j <= nkb; ++j) {
+                if (j < nkb) {
+                    const int st = j & 1;
+                    if (!mbar_wait_bounded(b_kvf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL, 2002, j) ||
+                        (j >= 2 && !mbar_wait_bounded(b_spfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
+                                                      limit, DEV_TIMEOUT_MMA_ACC, 2003, j))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbuf = sK + st * C::KT, vbuf = sV + st * C::KT;
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t aq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
+                        const uint32_t bk = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
+                        umma_bf16(tmem + 128u * st, desc_k(sQ + aq), desc_k(kbuf + bk), C::IDESC_S, k > 0);
+                        umma_bf16(tmem + 128u * st + 64u, desc_k(sdO + aq), desc_k(vbuf + bk), C::IDESC_S, k > 0);
+                    }
+                    any = true;
+                    umma_commit(b_spf + 8 * st);
+                }
+                if (j >= 1) {
+                    const int pj = j - 1, pst = pj & 1;
+                    if (!mbar_wait_bounded(b_dsf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_ACC, 2004, pj)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dsbuf = sdS + pst * C::ST, kbuf = sK + pst * C::KT;
+#pragma unroll
+                    for (int k = 0; k < C::BKV / 16; ++k)
+                        umma_bf16(tmem + C::DQ_COL, desc_k(dsbuf + 32u * k), desc_mn(kbuf + 2048u * k, C::KT / 2),
+                                  C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(b_kve + 8 * pst);
+                }
+            }
+            if (ok && any) umma_commit(b_dq);
+            if (!ok && any) drain_mma(b_drain, args.status);
+        }
+    } else {
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const int qi = q0 + r;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const size_t li = static_cast<size_t>(bh) * s + qi;
+        const float Lq = qi < s ? args.lse[li] : 0.0f;
+        const float Dq = qi < s ? args.delta[li] : 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkb; ++j) {
+            const int st = j & 1;
+            if (!warp_wait(b_spf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2005, j)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float p[C::BKV], dp[C::BKV];
+            {
+                uint32_t u[32];
+#pragma unroll
+                for (int c = 0; c < C::BKV / 32; ++c) {
+                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) p[32 * c + e] = __uint_as_float(u[e]);
+                    tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + 32u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dp[32 * c + e] = __uint_as_float(u[e]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_spfree + 8 * st);
+            const int kk0 = j * C::BKV;
+            const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
+#pragma unroll
+            for (int c = 0; c < C::BKV; ++c) {
+                float pv = ex2(fmaf(p[c], args.scale_log2, -Lq));
+                if (need_mask) {
+                    const int key = kk0 + c;
+                    if (qi >= s || key >= s || (args.causal && key > qi)) pv = 0.0f;
+                }
+                dp[c] = pv * (dp[c] - Dq);
+            }
+            if (j >= 2 && !warp_wait(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                     DEV_TIMEOUT_EPILOGUE, 2006, j)) {
+                ok = false;
+                break;
+            }
+            store_row_sw128<C::BKV, C::BQ>(sdS + st * C::ST, r, dp);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dsf + 8 * st);
+        }
+        if (ok && nkb > 0 && warp_wait(b_dq, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2007, -1)) {
+            tc_fence_after();
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * (3 * hd) + colQ;
+            uint32_t o[32];
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::DQ_COL + 32u * c, o);
+                tmem_ld_wait();
+                if (qi < s) store32_global(dst + 32 * c, o, args.scale);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---- D = rowsum(dC * C) per (token, head) ----------------------------------------------------
+
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const __nv_bfloat16* __restrict__ dC,
+                                                          const __nv_bfloat16* __restrict__ Cc, int T, int s, int a,
+                                                          float* __restrict__ D)
+{
+    const int lane = threadIdx.x & 31;
+    const long long total = static_cast<long long>(T) * a;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
+        const long long t = w / a;
+        const int head = static_cast<int>(w % a);
+        const size_t off = static_cast<size_t>(t) * a * kHeadDim + static_cast<size_t>(head) * kHeadDim + 4 * lane;
+        const uint2 u = *reinterpret_cast<const uint2*>(dC + off);
+        const uint2 v = *reinterpret_cast<const uint2*>(Cc + off);
+        const uint32_t uu[2] = {u.x, u.y}, vv[2] = {v.x, v.y};
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            acc = fmaf(__uint_as_float(uu[i] << 16), __uint_as_float(vv[i] << 16), acc);
+            acc = fmaf(__uint_as_float(uu[i] & 0xFFFF0000u), __uint_as_float(vv[i] & 0xFFFF0000u), acc);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            const long long bi = t / s, p = t % s;
+            D[(bi * a + head) * s + p] = acc;
+        }
+    }
+}
+
+template <typename Cfg, typename K>
+cudaError_t launch_tile_kernel(K kern, const AttnArgs& args, int blocks_y, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    if (blocks_y <= 0 || args.b * args.a <= 0) return cudaSuccess;
+    kern<<<dim3(args.b * args.a, blocks_y), 192, Cfg::SMEM_BYTES, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& args, cudaStream_t stream)
+{
+    return launch_tile_kernel<FwdCfg>(attn_fwd_kernel, args, (args.s + FwdCfg::BQ - 1) / FwdCfg::BQ, stream);
+}
+
+cudaError_t launch_attn_bwd_dq(const AttnArgs& args, cudaStream_t stream)
+{
+    return launch_tile_kernel<DqCfg>(attn_bwd_dq_kernel, args, (args.s + DqCfg::BQ - 1) / DqCfg::BQ, stream);
+}
+
+cudaError_t launch_attn_bwd_dkdv(const AttnArgs& args, cudaStream_t stream)
+{
+    return launch_tile_kernel<DkdvCfg>(attn_bwd_dkdv_kernel, args, (args.s + DkdvCfg::BKV - 1) / DkdvCfg::BKV, stream);
+}
+
+cudaError_t launch_attn_bwd_dot(const __nv_bfloat16* dC, const __nv_bfloat16* Cc, int T, int s, int a, float* D,
+                                int num_sms, cudaStream_t stream)
+{
+    const long long warps = static_cast<long long>(T) * a;
+    if (warps <= 0) return cudaSuccess;
+    long long blocks = (warps + 7) / 8;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    attn_bwd_dot_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(dC, Cc, T, s, a, D);
+    return cudaGetLastError();
+}
+
+}  // namespace mlp

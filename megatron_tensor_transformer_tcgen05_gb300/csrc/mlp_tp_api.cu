@@ -10,6 +10,7 @@
 #include <mutex>
 #include <vector>
 
+#include "attn_args.h"
 #include "colsum.cuh"
 #include "dropout.cuh"
 #include "gemm_args.h"
@@ -245,7 +246,7 @@ const char* mlp_tp_status_string(mlp_status s)
     switch (s) {
     case MLP_OK: return "MLP_OK";
     case MLP_EINVAL: return "MLP_EINVAL: null pointer or non-positive size";
-    case MLP_ESHAPE: return "MLP_ESHAPE: f % t != 0, or h, f, f/t not multiples of 8";
+    case MLP_ESHAPE: return "MLP_ESHAPE: a size breaks the call's shape rules (f % t, multiples of 8, a % t, d)";
     case MLP_EALIGN: return "MLP_EALIGN: pointer not 16-byte aligned";
     case MLP_ECUDA: return "MLP_ECUDA: CUDA runtime error";
     case MLP_ETIMEOUT: return "MLP_ETIMEOUT: a bounded device wait ran out";
@@ -569,7 +570,11 @@ const char* mlp_tp_kernel_name(int kernel)
     static const char* names[MLP_NUM_KERNELS] = {
         "gemm_fwd_up (H=XA+a, G=GELU(H))", "gemm_fwd_down (Y=GB+b)", "gemm_bwd_dh (dH=dY B^T * GELU'(H))",
         "gemm_bwd_dx (dX=dH A^T)",          "gemm_bwd_da (dA=X^T dH)", "gemm_bwd_db (dB=G^T dY)",
-        "colsum_partial (db)",              "bias_grad_finalize (da, db)", "dropout_backward (dY)"};
+        "colsum_partial (db)",              "bias_grad_finalize (da, db)", "dropout_backward (dY)",
+        "attn gemm_qkv (QKV=X Wqkv)",       "attn_fwd (C, L per head)",    "attn gemm_out (Y=C Wo)",
+        "attn gemm_dc (dC=dY Wo^T)",        "attn gemm_dwo (dWo=C^T dY)",  "attn_bwd_dot (D=rowsum dC*C)",
+        "attn_bwd_dq (dQ)",                 "attn_bwd_dkdv (dK, dV)",      "attn gemm_dx (dX=dQKV Wqkv^T)",
+        "attn gemm_dwqkv (dWqkv=X^T dQKV)"};
     return (kernel >= 0 && kernel < MLP_NUM_KERNELS) ? names[kernel] : "unknown";
 }
 
@@ -800,5 +805,198 @@ extern "C" mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
     colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    return MLP_OK;
+}
+
+// ---- head-parallel self-attention block ---------------------------------------------------
+
+namespace mlp {
+
+static mlp_status check_attn(int b, int s, int h, int a, int d, int t)
+{
+    if (b < 0 || s < 1 || h < 8 || a < 1 || d < 1 || t < 1) return MLP_EINVAL;
+    if (h % 8 != 0 || d != kHeadDim || a % t != 0) return MLP_ESHAPE;
+    if (static_cast<long long>(b) * s > 0x7fffffffLL || static_cast<long long>(a) * d * 3 > 0x7fffffffLL)
+        return MLP_EINVAL;
+    return MLP_OK;
+}
+
+static AttnArgs attn_args(const DeviceInfo* dev, int b, int s, int a, int causal)
+{
+    AttnArgs at{};
+    at.b = b;
+    at.s = s;
+    at.a = a;
+    at.causal = causal ? 1 : 0;
+    at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kHeadDim)));
+    at.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
+    at.status = dev->status;
+    at.timeout_ns = kWaitLimitNs;
+    return at;
+}
+
+static size_t attn_ws_dc(int T, int hd) { return round256(static_cast<size_t>(T) * hd * 2); }
+static size_t attn_ws_d(int b, int a, int s) { return round256(static_cast<size_t>(b) * a * s * 4); }
+
+}  // namespace mlp
+
+extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo, int b, int s,
+                                          int h, int a, int d, int t, int causal, mlp_bf16* QKV, mlp_bf16* Cctx,
+                                          float* L, mlp_bf16* Y, void* cuda_stream)
+{
+    mlp_status st = check_attn(b, s, h, a, d, t);
+    if (st != MLP_OK) return st;
+    if (!Wqkv || !Wo || (b > 0 && (!X || !QKV || !Cctx || !L || !Y))) return MLP_EINVAL;
+    const void* ptrs[] = {X, Wqkv, Wo, QKV, Cctx, L, Y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    if (b == 0) return MLP_OK;
+    cudaStream_t strm = static_cast<cudaStream_t>(cuda_stream);
+    const int T = b * s, hd = a * d;
+    CallTimer timer(strm);
+
+    // QKV = X Wqkv: every head of every shard in one GEMM (N = 3 a d).
+    GemmArgs g1{};
+    if (!map_kmajor(&g1.tmA, X, h, T, 128) || !map_mnmajor(&g1.tmB, Wqkv, 3 * hd, h) ||
+        !map_store(&g1.tmD0, QKV, 3 * hd, T))
+        return MLP_ECUDA;
+    g1.M = T; g1.N = 3 * hd; g1.K = h;
+    g1.status = dev->status;
+    g1.timeout_ns = kWaitLimitNs;
+    if (gemm<false, true, EPI_PLAIN>(g1, tile_n(3 * hd), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_QKV);
+
+    // Per head: scores, mask, softmax and P V on chip; C and L to HBM.
+    AttnArgs at = attn_args(dev, b, s, a, causal);
+    if (!make_map(&at.tmQ, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return MLP_ECUDA;
+    at.tmKV = at.tmQ;
+    at.out = reinterpret_cast<__nv_bfloat16*>(Cctx);
+    at.lse = L;
+    if (launch_attn_fwd(at, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_FWD);
+
+    // Y = C Wo: the sum over the t head shards is the K loop of one accumulator (K = a d).
+    GemmArgs g2{};
+    if (!map_kmajor(&g2.tmA, Cctx, hd, T, 128) || !map_mnmajor(&g2.tmB, Wo, h, hd) || !map_store(&g2.tmD0, Y, h, T))
+        return MLP_ECUDA;
+    g2.M = T; g2.N = h; g2.K = hd;
+    g2.status = dev->status;
+    g2.timeout_ns = kWaitLimitNs;
+    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_OUT);
+    return MLP_OK;
+}
+
+extern "C" size_t mlp_tp_attn_workspace_bytes(int b, int s, int h, int a, int d, int t)
+{
+    if (check_attn(b, s, h, a, d, t) != MLP_OK) return 0;
+    const int T = b * s, hd = a * d;
+    return attn_ws_dc(T, hd) + attn_ws_d(b, a, s) + round256(static_cast<size_t>(T) * 3 * hd * 2);
+}
+
+extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo,
+                                           const mlp_bf16* QKV, const mlp_bf16* Cctx, const float* L,
+                                           const mlp_bf16* dY, int b, int s, int h, int a, int d, int t, int causal,
+                                           mlp_bf16* dX, mlp_bf16* dWqkv, mlp_bf16* dWo, void* workspace,
+                                           size_t workspace_bytes, void* cuda_stream)
+{
+    mlp_status st = check_attn(b, s, h, a, d, t);
+    if (st != MLP_OK) return st;
+    if (!Wqkv || !Wo || !dWqkv || !dWo || !workspace || (b > 0 && (!X || !QKV || !Cctx || !L || !dY || !dX)))
+        return MLP_EINVAL;
+    const void* ptrs[] = {X, Wqkv, Wo, QKV, Cctx, L, dY, dX, dWqkv, dWo};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
+    if (workspace_bytes < mlp_tp_attn_workspace_bytes(b, s, h, a, d, t)) return MLP_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLP_OK) return st;
+    cudaStream_t strm = static_cast<cudaStream_t>(cuda_stream);
+    const int T = b * s, hd = a * d;
+    if (T == 0) {
+        if (cudaMemsetAsync(dWqkv, 0, static_cast<size_t>(h) * 3 * hd * 2, strm) != cudaSuccess ||
+            cudaMemsetAsync(dWo, 0, static_cast<size_t>(hd) * h * 2, strm) != cudaSuccess)
+            return MLP_ECUDA;
+        return MLP_OK;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mlp_bf16* dC = reinterpret_cast<mlp_bf16*>(ws);
+    float* D = reinterpret_cast<float*>(ws + attn_ws_dc(T, hd));
+    mlp_bf16* dQKV = reinterpret_cast<mlp_bf16*>(ws + attn_ws_dc(T, hd) + attn_ws_d(b, a, s));
+    CallTimer timer(strm);
+
+    // dC = dY Wo^T (each head shard's rows of Wo).
+    GemmArgs g3{};
+    const int bn_hd = tile_n(hd);
+    if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, Wo, h, hd, kmajor_b_box(T, bn_hd)) ||
+        !map_store(&g3.tmD0, dC, hd, T))
+        return MLP_ECUDA;
+    g3.M = T; g3.N = hd; g3.K = h;
+    g3.status = dev->status;
+    g3.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_PLAIN>(g3, bn_hd, dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DC);
+
+    // dWo = C^T dY.
+    GemmArgs g4{};
+    if (!map_mnmajor(&g4.tmA, Cctx, hd, T) || !map_mnmajor(&g4.tmB, dY, h, T) || !map_store(&g4.tmD0, dWo, h, hd))
+        return MLP_ECUDA;
+    g4.M = hd; g4.N = h; g4.K = T;
+    g4.status = dev->status;
+    g4.timeout_ns = kWaitLimitNs;
+    if (gemm<true, true, EPI_PLAIN>(g4, tile_n(h), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DWO);
+
+    // D = rowsum(dC (.) C) per (token, head).
+    if (launch_attn_bwd_dot(reinterpret_cast<const __nv_bfloat16*>(dC), reinterpret_cast<const __nv_bfloat16*>(Cctx),
+                            T, s, a, D, dev->num_sms, strm) != cudaSuccess)
+        return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DOT);
+
+    // dQ: per 128-query block over 64-key blocks.
+    AttnArgs aq = attn_args(dev, b, s, a, causal);
+    if (!make_map(&aq.tmQ, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&aq.tmKV, QKV, 3 * hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&aq.tmdO, dC, hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLP_ECUDA;
+    aq.out = reinterpret_cast<__nv_bfloat16*>(dQKV);
+    aq.lse = const_cast<float*>(L);
+    aq.delta = D;
+    if (launch_attn_bwd_dq(aq, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DQ);
+
+    // dK, dV: per 128-key block over 64-query blocks.
+    AttnArgs ak = aq;
+    if (!make_map(&ak.tmKV, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&ak.tmQ, QKV, 3 * hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&ak.tmdO, dC, hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLP_ECUDA;
+    if (launch_attn_bwd_dkdv(ak, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DKDV);
+
+    // dX = dQKV Wqkv^T: one accumulator over K = 3 a d sums Q, K, V and all head shards.
+    GemmArgs g6{};
+    const int bn_h = tile_n(h);
+    if (!map_kmajor(&g6.tmA, dQKV, 3 * hd, T, 128) || !map_kmajor(&g6.tmB, Wqkv, 3 * hd, h, kmajor_b_box(T, bn_h)) ||
+        !map_store(&g6.tmD0, dX, h, T))
+        return MLP_ECUDA;
+    g6.M = T; g6.N = h; g6.K = 3 * hd;
+    g6.status = dev->status;
+    g6.timeout_ns = kWaitLimitNs;
+    if (gemm<false, false, EPI_PLAIN>(g6, bn_h, dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DX);
+
+    // dWqkv = X^T dQKV.
+    GemmArgs g7{};
+    if (!map_mnmajor(&g7.tmA, X, h, T) || !map_mnmajor(&g7.tmB, dQKV, 3 * hd, T) ||
+        !map_store(&g7.tmD0, dWqkv, 3 * hd, h))
+        return MLP_ECUDA;
+    g7.M = h; g7.N = 3 * hd; g7.K = T;
+    g7.status = dev->status;
+    g7.timeout_ns = kWaitLimitNs;
+    if (gemm<true, true, EPI_PLAIN>(g7, tile_n(3 * hd), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    timer.mark(MLP_K_ATTN_DWQKV);
     return MLP_OK;
 }

@@ -111,3 +111,72 @@ def make_any_inputs(w: Workload, *, seed: int = 0) -> dict[str, torch.Tensor]:
     if w.kind == "swiglu":
         return make_swiglu_inputs(w.T, w.h, w.f, seed=seed, sx=w.sx, sw=w.sw, sdy=w.sdy)
     return make_workload_inputs(w, seed=seed)
+
+
+# ---- head-parallel attention block ----------------------------------------------------------
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Head-parallel self-attention at a GPT layer shape: b sequences of s tokens, hidden
+    width h, a heads of width d = h / a, split over t shards; causal mask (GPT)."""
+    name: str
+    b: int
+    s: int
+    h: int
+    a: int
+    t: int
+    causal: bool = True
+    sx: float = 1.0
+    sw: float = 0.02
+    sdy: float = 0.01
+    desc: str = ""
+    kind: str = "attention"
+
+    @property
+    def d(self) -> int:
+        return self.h // self.a
+
+    @property
+    def T(self) -> int:
+        return self.b * self.s
+
+    @property
+    def flops_fwd_bwd(self) -> int:
+        """Matmul FLOPs of one forward + backward. Projections: X Wqkv and C Wo forward
+        (8 T h (a d)), twice that backward. Attention core per head: Q K^T and P V forward
+        (2 s^2 d each over the unmasked pairs), dP, dV, dQ, dK backward (2.5x the forward);
+        only the s (s + 1) / 2 unmasked pairs count when causal."""
+        hd = self.a * self.d
+        pairs = self.s * (self.s + 1) // 2 if self.causal else self.s * self.s
+        return 24 * self.T * self.h * hd + 14 * self.b * self.a * pairs * self.d
+
+
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {w.name: w for w in [
+    AttnWorkload("attn-tiny", 2, 200, 256, 2, 2, sw=0.08, sdy=1.0,
+                 desc="tiny head-parallel attention b=2 s=200 h=256 a=2 d=128 t=2, causal"),
+    AttnWorkload("gpt-18b-attn", 4, 2048, 6144, 48, 8,
+                 desc="GPT 18B-shaped attention b=4 s=2048 h=6144 a=48 d=128 t=8, causal"),
+    AttnWorkload("gpt3-175b-attn", 2, 2048, 12288, 96, 8,
+                 desc="GPT-3 175B-shaped attention b=2 s=2048 h=12288 a=96 d=128 t=8, causal"),
+]}
+
+
+def make_attn_inputs(b: int, s: int, h: int, a: int, d: int, *, seed: int = 0, sx: float = 1.0, sw: float = 0.02,
+                     sdy: float = 0.01) -> dict[str, torch.Tensor]:
+    """Inputs of the attention block, drawn in the order X, Wq, Wk, Wv, Wo, dY (same recipe).
+    "Wqkv" is Wq, Wk and Wv side by side ([h, 3 a d]), the layout the C ABI takes."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    T, hd = b * s, a * d
+    shp = {"X": (T, h), "Wq": (h, hd), "Wk": (h, hd), "Wv": (h, hd), "Wo": (hd, h), "dY": (T, h)}
+    sig = {"X": sx, "Wq": sw, "Wk": sw, "Wv": sw, "Wo": sw, "dY": sdy}
+    out = {}
+    for name, sh in shp.items():
+        v = torch.randn(sh, generator=g, dtype=torch.float32)
+        v.mul_(sig[name])
+        out[name] = v.to(torch.bfloat16)
+    out["Wqkv"] = torch.cat([out["Wq"], out["Wk"], out["Wv"]], dim=1).contiguous()
+    return out
+
+
+def make_attn_workload_inputs(w: AttnWorkload, *, seed: int = 0) -> dict[str, torch.Tensor]:
+    return make_attn_inputs(w.b, w.s, w.h, w.a, w.d, seed=seed, sx=w.sx, sw=w.sw, sdy=w.sdy)

@@ -76,11 +76,14 @@ def _load():
             lib.oracle_swiglu_sampled_bf16.restype = i32
             lib.oracle_swiglu_sampled_bf16.argtypes = [i64, i64, i64] + [dp] * 5 + [i64, dp, i64, dp] + [dp] * 5
             lib.oracle_attn_forward.restype = i32
-            lib.oracle_attn_forward.argtypes = [i64] * 5 + [i32] + [dp] * 11
+            lib.oracle_attn_forward.argtypes = [i64] * 5 + [i32] + [dp] * 12
             lib.oracle_attn_backward.restype = i32
             lib.oracle_attn_backward.argtypes = [i64] * 5 + [dp] * 16
             lib.oracle_attn_sharded.restype = i32
             lib.oracle_attn_sharded.argtypes = [i64] * 6 + [i32] + [dp] * 14
+            lib.oracle_attn_sampled_bf16.restype = i32
+            lib.oracle_attn_sampled_bf16.argtypes = ([i64] * 5 + [i32] + [ctypes.c_void_p] * 5 + [i64, ctypes.c_void_p, i64]
+                                                     + [dp] * 2)
             lib.oracle_swiglu_sharded.restype = i32
             lib.oracle_swiglu_sharded.argtypes = [i64, i64, i64, i64] + [dp] * 12
             _lib = lib
@@ -349,8 +352,9 @@ def attn_fwd_bwd(inp: dict, b: int, s: int, a: int, causal: bool = True) -> dict
     o = {k: np.empty((T, hd)) for k in ("Q", "K", "V", "C")}
     o["P"] = np.empty((b, a, s, s))
     o["Y"] = np.empty((T, h))
+    o["L"] = np.empty((b * a, s))
     rc = lib.oracle_attn_forward(b, s, h, a, d, int(causal), _p(X), _p(Wq), _p(Wk), _p(Wv), _p(Wo), _p(o["Q"]),
-                                 _p(o["K"]), _p(o["V"]), _p(o["P"]), _p(o["C"]), _p(o["Y"]))
+                                 _p(o["K"]), _p(o["V"]), _p(o["P"]), _p(o["C"]), _p(o["Y"]), _p(o["L"]))
     assert rc == 0, rc
     o.update(dX=np.empty((T, h)), dWq=np.empty((h, hd)), dWk=np.empty((h, hd)), dWv=np.empty((h, hd)),
              dWo=np.empty((hd, h)))
@@ -379,3 +383,21 @@ def attn_sharded(inp: dict, b: int, s: int, a: int, t: int, causal: bool = True,
     if parts:
         o["Y_part"], o["dX_part"] = Yp, dXp
     return o
+
+
+def attn_sampled_bf16(inp: dict, b: int, s: int, a: int, rows, heads, causal: bool = True) -> dict:
+    """C[rows, heads] ([n_rows, n_heads, d]) and L[rows, heads] from the bf16 inputs, without
+    computing the whole block (sampled outputs at full size)."""
+    lib = _load()
+    X, Wq, Wk, Wv = (_bits(inp[k]) for k in ("X", "Wq", "Wk", "Wv"))
+    T, h = X.shape
+    hd = Wq.shape[1]
+    d = hd // a
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    heads = np.ascontiguousarray(heads, dtype=np.int64)
+    C = np.empty((len(rows), len(heads), d))
+    L = np.empty((len(rows), len(heads)))
+    rc = lib.oracle_attn_sampled_bf16(b, s, h, a, d, int(causal), _p(X), _p(Wq), _p(Wk), _p(Wv), _p(rows), len(rows),
+                                      _p(heads), len(heads), _p(C), _p(L))
+    assert rc == 0, rc
+    return {"C": C, "L": L}

@@ -660,7 +660,7 @@ int oracle_swiglu_sampled_bf16(int64_t T, int64_t h, int64_t f, const uint16_t *
  *   Y = C Wo                                                     [T, h]
  * with a heads of width d (hd = a*d columns; the pages use hd = h). No biases. */
 static void attn_core_forward(int64_t b, int64_t s, int64_t a, int64_t d, int causal, const double *Q,
-                              const double *K, const double *V, double *P, double *C)
+                              const double *K, const double *V, double *P, double *C, double *L)
 {
     const int64_t hd = a * d;
     const double scale = 1.0 / sqrt((double)d);
@@ -689,6 +689,8 @@ static void attn_core_forward(int64_t b, int64_t s, int64_t a, int64_t d, int ca
                     sum += e;
                 }
                 for (int64_t j = 0; j < s; ++j) Pbh[i * s + j] /= sum;
+                /* base-2 log-sum-exp of the row's scaled scores: log2 sum_j exp(S_ij) */
+                if (L) L[(bi * a + hh) * s + i] = (m + log(sum)) / log(2.0);
                 double *c = C + (bi * s + i) * hd + hh * d;
                 for (int64_t e = 0; e < d; ++e) c[e] = 0.0;
                 for (int64_t j = 0; j < s; ++j) {
@@ -703,14 +705,14 @@ static void attn_core_forward(int64_t b, int64_t s, int64_t a, int64_t d, int ca
 
 int oracle_attn_forward(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, int causal, const double *X,
                         const double *Wq, const double *Wk, const double *Wv, const double *Wo, double *Q,
-                        double *K, double *V, double *P, double *C, double *Y)
+                        double *K, double *V, double *P, double *C, double *Y, double *L)
 {
     if (b < 1 || s < 1 || h < 1 || a < 1 || d < 1) return 1;
     const int64_t T = b * s, hd = a * d;
     mm_nn(T, hd, h, X, Wq, Q);
     mm_nn(T, hd, h, X, Wk, K);
     mm_nn(T, hd, h, X, Wv, V);
-    attn_core_forward(b, s, a, d, causal, Q, K, V, P, C);
+    attn_core_forward(b, s, a, d, causal, Q, K, V, P, C, L);
     mm_nn(T, h, hd, C, Wo, Y);
     return 0;
 }
@@ -807,7 +809,7 @@ int oracle_attn_sharded(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, i
             }
         for (int64_t c = 0; c < cs; ++c)
             for (int64_t n = 0; n < h; ++n) o[c * h + n] = Wo[(c0 + c) * h + n];
-        oracle_attn_forward(b, s, h, as, d, causal, X, q, k, v, o, Qi, Ki, Vi, Pi, Ci, Yi);
+        oracle_attn_forward(b, s, h, as, d, causal, X, q, k, v, o, Qi, Ki, Vi, Pi, Ci, Yi, NULL);
         for (int64_t e = 0; e < T * h; ++e) Y[e] += Yi[e];
         if (Y_part) memcpy(Y_part + sh * T * h, Yi, sizeof(double) * nth);
         oracle_attn_backward(b, s, h, as, d, X, q, k, v, o, Qi, Ki, Vi, Pi, Ci, dY, dXi, gq, gk, gv, go);
@@ -824,5 +826,84 @@ int oracle_attn_sharded(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, i
     }
     free(q); free(k); free(v); free(o); free(Qi); free(Ki); free(Vi); free(Ci); free(Pi); free(Yi); free(dXi);
     free(gq); free(gk); free(gv); free(go);
+    return 0;
+}
+
+/* Sampled attention outputs at sizes where the whole block is too slow on a CPU: for each
+ * listed head and token row, C[row, head] (d values) and L[row, head], from bf16 inputs
+ * (raw bits). For every (sequence, head) touched, K and V of the head are computed over the
+ * positions the sampled rows can see, then each row's scores, softmax and P V, all fp64. */
+int oracle_attn_sampled_bf16(int64_t b, int64_t s, int64_t h, int64_t a, int64_t d, int causal, const uint16_t *X,
+                             const uint16_t *Wq, const uint16_t *Wk, const uint16_t *Wv, const int64_t *rows,
+                             int64_t nrows, const int64_t *heads, int64_t nheads, double *C_out, double *L_out)
+{
+    if (b < 1 || s < 1 || h < 1 || a < 1 || d < 1) return 1;
+    const int64_t hd = a * d, T = b * s;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= T) return 1;
+    for (int64_t k = 0; k < nheads; ++k)
+        if (heads[k] < 0 || heads[k] >= a) return 1;
+    double *Wcol = malloc(sizeof(double) * (size_t)(h * d * 3));
+    double *Kh = malloc(sizeof(double) * (size_t)(s * d)), *Vh = malloc(sizeof(double) * (size_t)(s * d));
+    double *sc = malloc(sizeof(double) * (size_t)s), *q = malloc(sizeof(double) * (size_t)d);
+    if (!Wcol || !Kh || !Vh || !sc || !q) return 2;
+    const double scale = 1.0 / sqrt((double)d);
+    for (int64_t hk = 0; hk < nheads; ++hk) {
+        const int64_t hh = heads[hk], c0 = hh * d;
+        for (int64_t i = 0; i < h; ++i)
+            for (int64_t e = 0; e < d; ++e) {
+                Wcol[(0 * h + i) * d + e] = bf16d(Wq[i * hd + c0 + e]);
+                Wcol[(1 * h + i) * d + e] = bf16d(Wk[i * hd + c0 + e]);
+                Wcol[(2 * h + i) * d + e] = bf16d(Wv[i * hd + c0 + e]);
+            }
+        for (int64_t bi = 0; bi < b; ++bi) {
+            int64_t pmax = -1;
+            for (int64_t r = 0; r < nrows; ++r)
+                if (rows[r] / s == bi) {
+                    const int64_t p = rows[r] % s;
+                    const int64_t need = causal ? p : s - 1;
+                    if (need > pmax) pmax = need;
+                }
+            if (pmax < 0) continue;
+#pragma omp parallel for schedule(static)
+            for (int64_t p = 0; p <= pmax; ++p) {
+                const uint16_t *x = X + (bi * s + p) * h;
+                for (int64_t e = 0; e < d; ++e) { Kh[p * d + e] = 0.0; Vh[p * d + e] = 0.0; }
+                for (int64_t i = 0; i < h; ++i) {
+                    const double xv = bf16d(x[i]);
+                    const double *wk = Wcol + (1 * h + i) * d, *wv = Wcol + (2 * h + i) * d;
+                    for (int64_t e = 0; e < d; ++e) {
+                        Kh[p * d + e] += xv * wk[e];
+                        Vh[p * d + e] += xv * wv[e];
+                    }
+                }
+            }
+            for (int64_t r = 0; r < nrows; ++r) {
+                if (rows[r] / s != bi) continue;
+                const int64_t p = rows[r] % s, nk = causal ? p + 1 : s;
+                const uint16_t *x = X + rows[r] * h;
+                for (int64_t e = 0; e < d; ++e) q[e] = 0.0;
+                for (int64_t i = 0; i < h; ++i) {
+                    const double xv = bf16d(x[i]);
+                    for (int64_t e = 0; e < d; ++e) q[e] += xv * Wcol[(0 * h + i) * d + e];
+                }
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nk; ++j) {
+                    double dot = 0.0;
+                    for (int64_t e = 0; e < d; ++e) dot += q[e] * Kh[j * d + e];
+                    sc[j] = dot * scale;
+                    if (sc[j] > m) m = sc[j];
+                }
+                double sum = 0.0;
+                for (int64_t j = 0; j < nk; ++j) { sc[j] = exp(sc[j] - m); sum += sc[j]; }
+                double *c = C_out + (r * nheads + hk) * d;
+                for (int64_t e = 0; e < d; ++e) c[e] = 0.0;
+                for (int64_t j = 0; j < nk; ++j)
+                    for (int64_t e = 0; e < d; ++e) c[e] += sc[j] / sum * Vh[j * d + e];
+                L_out[r * nheads + hk] = (m + log(sum)) / log(2.0);
+            }
+        }
+    }
+    free(Wcol); free(Kh); free(Vh); free(sc); free(q);
     return 0;
 }

@@ -99,3 +99,33 @@ def test_uniform_scores_closed_form():
     np.testing.assert_allclose(out["Y"], one["X"] @ one["Wv"] @ one["Wo"], rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(out["dWq"], 0.0, atol=1e-15)  # a lone score has zero softmax gradient
     np.testing.assert_allclose(out["dWk"], 0.0, atol=1e-15)
+
+
+def test_lse_reproduces_the_probabilities():
+    """L is the base-2 log-sum-exp of the scaled scores: 2^(S log2 e - L) gives back P."""
+    b, s, h, a, d = 2, 6, 5, 2, 3
+    inp = _rand(b, s, h, a, d, seed=7)
+    out = oracle.attn_fwd_bwd(inp, b, s, a, causal=True)
+    for bi in range(b):
+        for hh in range(a):
+            rows = slice(bi * s, (bi + 1) * s)
+            cols = slice(hh * d, (hh + 1) * d)
+            S = out["Q"][rows, cols] @ out["K"][rows, cols].T / np.sqrt(d)
+            P = np.where(np.tril(np.ones((s, s))) > 0, np.exp2(S * np.log2(np.e) - out["L"][bi * a + hh][:, None]), 0)
+            np.testing.assert_allclose(P, out["P"][bi, hh], rtol=1e-12, atol=1e-15)
+
+
+def test_sampled_bf16_matches_the_full_oracle():
+    """The sampled C and L agree with the full forward on bf16-representable inputs."""
+    import torch
+    from megatron_tensor_transformer_tcgen05_gb300.inputs import make_attn_inputs
+    b, s, h, a, d = 2, 9, 16, 2, 4
+    inp = make_attn_inputs(b, s, h, a, d, seed=3, sw=0.3)
+    full = oracle.attn_fwd_bwd({k: v.double().numpy() for k, v in inp.items()}, b, s, a, causal=True)
+    rows, heads = np.array([0, 4, 8, 9, 17]), np.array([1, 0])
+    smp = oracle.attn_sampled_bf16(inp, b, s, a, rows, heads, causal=True)
+    for ri, r in enumerate(rows):
+        for hi, hh in enumerate(heads):
+            np.testing.assert_allclose(smp["C"][ri, hi], full["C"][r, hh * d:(hh + 1) * d], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(smp["L"][ri, hi], full["L"][(r // s) * a + hh, r % s], rtol=1e-13)
+    assert torch.is_tensor(inp["X"])
