@@ -142,13 +142,16 @@ class AttnWorkload:
 
     @property
     def flops_fwd_bwd(self) -> int:
-        """Matmul FLOPs of one forward + backward. Projections: X Wqkv and C Wo forward
-        (8 T h (a d)), twice that backward. Attention core per head: Q K^T and P V forward
-        (2 s^2 d each over the unmasked pairs), dP, dV, dQ, dK backward (2.5x the forward);
-        only the s (s + 1) / 2 unmasked pairs count when causal."""
-        hd = self.a * self.d
-        pairs = self.s * (self.s + 1) // 2 if self.causal else self.s * self.s
-        return 24 * self.T * self.h * hd + 14 * self.b * self.a * pairs * self.d
+        return attn_flops(self.b, self.s, self.h, self.a, self.d, self.causal)
+
+
+def attn_flops(b: int, s: int, h: int, a: int, d: int, causal: bool) -> int:
+    """Matmul FLOPs of one forward + backward of the attention block. Projections: X Wqkv
+    and C Wo forward (8 T h (a d)), twice that backward. Attention core per head: Q K^T and
+    P V forward (2 d FLOPs per query-key pair each), dP, dV, dQ, dK backward (2.5x the
+    forward); when causal only the s (s + 1) / 2 unmasked pairs count."""
+    pairs = s * (s + 1) // 2 if causal else s * s
+    return 24 * b * s * h * a * d + 14 * b * a * pairs * d
 
 
 ATTN_WORKLOADS: dict[str, AttnWorkload] = {w.name: w for w in [
