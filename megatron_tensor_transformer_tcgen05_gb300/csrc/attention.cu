@@ -9,11 +9,12 @@
 // mask implicit, section 4 "kernel fusion"). Here the whole of S -> P -> C also stays on
 // chip: S is never written to HBM.
 //
-// Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 192 threads.
-//   warp 0     TMA: the Q block once, then K and V blocks of 128 keys into a 2-stage ring
+// Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 320 threads.
+//   warp 0     TMA: the Q block once, then K and V blocks of 128 keys through a 4-slot ring
 //   warp 1     TMEM allocation and every tcgen05.mma: S_j = Q K_j^T into one of two TMEM
 //              S buffers, O += P_j V_j into the TMEM output accumulator
-//   warps 2-5  softmax, thread r <-> query row r (TMEM lane r): read S_j from TMEM, mask,
+//   warps 2-9  softmax, two threads per query row r (TMEM lane r), each on half of the
+//              block's columns: read S_j from TMEM, mask,
 //              running row max and sum (base 2), P_j -> shared memory (bf16, the A operand
 //              of the next MMA); rescale O in TMEM only when the row max has grown by more
 //              than 2^8 since the last rescale (the final division by the row sum makes the
@@ -87,6 +88,32 @@ __device__ __forceinline__ void store_row_sw128(uint32_t buf, int r, const float
         }
 }
 
+// Columns [c0, c0 + NC) of row r of the same layout (c0 a multiple of 8).
+template <int NC, int ROWS>
+__device__ __forceinline__ void store_row_part_sw128(uint32_t buf, int r, int c0, const float (&v)[NC])
+{
+#pragma unroll
+    for (int i = 0; i < NC / 8; ++i) {
+        const int c = c0 + 8 * i;
+        const uint32_t kc = static_cast<uint32_t>(c >> 6), u = static_cast<uint32_t>((c >> 3) & 7);
+        sts128(buf + kc * (ROWS * 128u) + static_cast<uint32_t>(r * 128) + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+               pack2_bf16(v[8 * i], v[8 * i + 1]), pack2_bf16(v[8 * i + 2], v[8 * i + 3]),
+               pack2_bf16(v[8 * i + 4], v[8 * i + 5]), pack2_bf16(v[8 * i + 6], v[8 * i + 7]));
+    }
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // 32 fp32 values * mul -> 32 bf16 at dst (64 bytes, 16-byte aligned).
 __device__ __forceinline__ void store32_global(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul)
 {
@@ -136,12 +163,41 @@ __device__ __forceinline__ void drain_mma(uint32_t bar, int* status)
 
 // ---- forward -------------------------------------------------------------------------------
 
+// Max and sum of N values through 8 independent partial results (short dependency chains).
+template <int N>
+__device__ __forceinline__ float max_tree(const float (&x)[N])
+{
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = x[i];
+#pragma unroll
+    for (int c = 8; c < N; ++c) m[c & 7] = fmaxf(m[c & 7], x[c]);
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+template <int N>
+__device__ __forceinline__ float sum_tree(const float (&x)[N])
+{
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = x[i];
+#pragma unroll
+    for (int c = 8; c < N; ++c) m[c & 7] += x[c];
+    return ((m[0] + m[1]) + (m[2] + m[3])) + ((m[4] + m[5]) + (m[6] + m[7]));
+}
+
 struct FwdCfg {
     static constexpr int BQ = 128, BKV = 128;
+    static constexpr int THREADS = 320;  // producer, MMA, 8 softmax warps (two threads per row)
     static constexpr uint32_t TILE = 128 * kHeadDim * 2;  // a 128 x 128 bf16 tile: 32 KB
-    static constexpr uint32_t OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE, OFF_BAR = 7 * TILE;
-    // barriers: q | kfull[2] | vfull[2] | kvempty[2] | sfull[2] | sfree[2] | pfull[2] | pvdone[2] | drain
-    static constexpr int NUM_BARS = 16;
+    // K and V blocks share one ring of slots, loaded K_0 V_0 K_1 V_1 ...; a K slot is freed as
+    // soon as its S MMA completes and a V slot when its PV MMA completes, so the loads run
+    // ahead of the softmax instead of waiting for the PV product.
+    static constexpr int SLOTS = 4;
+    static constexpr uint32_t OFF_Q = 0, OFF_KV = TILE, OFF_P = (1 + SLOTS) * TILE, OFF_X = (2 + SLOTS) * TILE,
+                              OFF_BAR = OFF_X + 2 * 2 * 128 * 4;
+    // barriers: q | full[4] | empty[4] | sfull[2] | sfree[2] | pfull | pvdone | drain | pair[4][2]
+    static constexpr int NUM_BARS = 1 + 2 * SLOTS + 4 + 3 + 8;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);
@@ -150,24 +206,28 @@ struct FwdCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = FwdCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V, sP = base + C::OFF_P;
+    const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV, sP = base + C::OFF_P, sX = base + C::OFF_X;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_q = bar, b_kf = bar + 8, b_vf = bar + 24, b_kve = bar + 40, b_sf = bar + 56, b_sfree = bar + 72,
-                   b_pf = bar + 88, b_pv = bar + 104, b_drain = bar + 120;
+    const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 8 * C::SLOTS, b_sf = b_empty + 8 * C::SLOTS,
+                   b_sfree = b_sf + 16, b_pf = b_sfree + 16, b_pv = b_pf + 8, b_drain = b_pv + 8,
+                   b_pair = b_drain + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = args.s, a = args.a;
-    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
-    const int qb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest rows first
+    // Head-major order: the query blocks of one head run side by side and share its K and V
+    // blocks through L2; within a head the longest rows start first.
+    const int nqb = (s + C::BQ - 1) / C::BQ;
+    const int bh = static_cast<int>(blockIdx.x) / nqb, bi = bh / a, head = bh % a;
+    const int qb = nqb - 1 - static_cast<int>(blockIdx.x) % nqb;
     const int q0 = qb * C::BQ;
     const int nkb_all = (s + C::BKV - 1) / C::BKV;
     const int nkb = args.causal ? min(nkb_all, qb + 1) : nkb_all;
@@ -178,16 +238,18 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(b_kf + 8 * i, 1);
-            mbar_init(b_vf + 8 * i, 1);
-            mbar_init(b_kve + 8 * i, 1);
-            mbar_init(b_sf + 8 * i, 1);
-            mbar_init(b_sfree + 8 * i, 4);
-            mbar_init(b_pf + 8 * i, 4);
-            mbar_init(b_pv + 8 * i, 1);
+        for (int i = 0; i < C::SLOTS; ++i) {
+            mbar_init(b_full + 8 * i, 1);
+            mbar_init(b_empty + 8 * i, 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_sf + 8 * i, 1);
+            mbar_init(b_sfree + 8 * i, 8);
+        }
+        mbar_init(b_pf, 8);
+        mbar_init(b_pv, 1);
         mbar_init(b_drain, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(b_pair + 8 * i, 2);  // the two warps of a row quadrant
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&args.tmQ);
@@ -205,31 +267,30 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
-            // barrier index for the drain: 0 = q, 1..2 = kfull, 3..4 = vfull
+            // drain indices: 0 = q, 1 + i = full[i]
             uint32_t issued = 1u, par = 0u;
             bool ok = true;
-            mbar_arrive_expect_tx(b_q, 2 * C::TILE / 2);
+            mbar_arrive_expect_tx(b_q, C::TILE);
             tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_q);
             tma_load_2d(sQ + C::TILE / 2, &args.tmQ, colQ + 64, row0 + q0, b_q);
-            for (int j = 0; j < nkb; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait_bounded(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                                 DEV_TIMEOUT_PRODUCER, 1000, j)) {
+            for (int n = 0; n < 2 * nkb; ++n) {  // n = 2j: K_j, n = 2j + 1: V_j
+                const int slot = n % C::SLOTS;
+                const uint32_t ph = static_cast<uint32_t>(n / C::SLOTS) & 1u;
+                if (n >= C::SLOTS && !mbar_wait_bounded(b_empty + 8 * slot, ph ^ 1u, abort_flag, args.status, limit,
+                                                        DEV_TIMEOUT_PRODUCER, 1000, n)) {
                     ok = false;
                     break;
                 }
-                const int y = row0 + j * C::BKV;
-                const uint32_t ph = (j >> 1) & 1;
-                mbar_arrive_expect_tx(b_kf + 8 * st, C::TILE);
-                tma_load_2d(sK + st * C::TILE, &args.tmKV, colK, y, b_kf + 8 * st);
-                tma_load_2d(sK + st * C::TILE + C::TILE / 2, &args.tmKV, colK + 64, y, b_kf + 8 * st);
-                mbar_arrive_expect_tx(b_vf + 8 * st, C::TILE);
-                tma_load_2d(sV + st * C::TILE, &args.tmKV, colV, y, b_vf + 8 * st);
-                tma_load_2d(sV + st * C::TILE + C::TILE / 2, &args.tmKV, colV + 64, y, b_vf + 8 * st);
-                issued |= (1u << (1 + st)) | (1u << (3 + st));
-                par = (par & ~((1u << (1 + st)) | (1u << (3 + st)))) | (ph << (1 + st)) | (ph << (3 + st));
+                const int y = row0 + (n >> 1) * C::BKV;
+                const int x = (n & 1) ? colV : colK;
+                const uint32_t dst = sKV + slot * C::TILE, fb = b_full + 8 * slot;
+                mbar_arrive_expect_tx(fb, C::TILE);
+                tma_load_2d(dst, &args.tmKV, x, y, fb);
+                tma_load_2d(dst + C::TILE / 2, &args.tmKV, x + 64, y, fb);
+                issued |= 1u << (1 + slot);
+                par = (par & ~(1u << (1 + slot))) | (ph << (1 + slot));
             }
-            if (!ok) drain_loads(bar, 5, issued, par, args.status);
+            if (!ok) drain_loads(bar, 1 + C::SLOTS, issued, par, args.status);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
@@ -237,9 +298,9 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
             bool ok = mbar_wait_bounded(b_q, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 1001, -1);
             bool any = false;
             for (int j = 0; ok && j <= nkb; ++j) {
-                if (j < nkb) {
-                    const int st = j & 1;
-                    if (!mbar_wait_bounded(b_kf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
+                if (j < nkb) {  // S_j = Q K_j^T
+                    const int st = j & 1, n = 2 * j, slot = n % C::SLOTS;
+                    if (!mbar_wait_bounded(b_full + 8 * slot, (n / C::SLOTS) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 1002, j) ||
                         (j >= 2 && !mbar_wait_bounded(b_sfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
                                                       limit, DEV_TIMEOUT_MMA_ACC, 1003, j))) {
@@ -247,7 +308,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbuf = sK + st * C::TILE;
+                    const uint32_t kbuf = sKV + slot * C::TILE;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t off = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
@@ -255,71 +316,89 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
                     }
                     any = true;
                     umma_commit(b_sf + 8 * st);
+                    umma_commit(b_empty + 8 * slot);
                 }
-                if (j >= 1) {
-                    const int pj = j - 1, pst = pj & 1;
-                    if (!mbar_wait_bounded(b_pf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_ACC, 1004, pj) ||
-                        !mbar_wait_bounded(b_vf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
+                if (j >= 1) {  // O += P_{j-1} V_{j-1}
+                    const int pj = j - 1, n = 2 * pj + 1, slot = n % C::SLOTS;
+                    if (!mbar_wait_bounded(b_pf, pj & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 1004,
+                                           pj) ||
+                        !mbar_wait_bounded(b_full + 8 * slot, (n / C::SLOTS) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 1005, pj)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t pbuf = sP + pst * C::TILE, vbuf = sV + pst * C::TILE;
+                    const uint32_t vbuf = sKV + slot * C::TILE;
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k) {
                         const uint32_t aoff = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + C::O_COL, desc_k(pbuf + aoff), desc_mn(vbuf + 2048u * k, C::TILE / 2),
+                        umma_bf16(tmem + C::O_COL, desc_k(sP + aoff), desc_mn(vbuf + 2048u * k, C::TILE / 2),
                                   C::IDESC_PV, (pj > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(b_pv + 8 * pst);
-                    umma_commit(b_kve + 8 * pst);
+                    umma_commit(b_pv);
+                    umma_commit(b_empty + 8 * slot);
                 }
             }
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
         // ------------------------------ softmax -----------------------------------
-        const int q = warp & 3;
+        // Two threads per query row: warp w (2..9) reads TMEM lanes of quadrant w % 4 and
+        // columns [64 half, 64 half + 64) of each block, half = (w - 2) / 4. The pair shares
+        // its row max through shared memory (double-buffered; an mbarrier per quadrant and
+        // buffer, waited with the usual bound), so both apply the same reference and rescale
+        // decisions.
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int qi = q0 + r;
+        const int cb = 64 * half;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t x_mine = sX + static_cast<uint32_t>((half * 128 + r) * 4);
+        const uint32_t x_peer = sX + static_cast<uint32_t>(((1 - half) * 128 + r) * 4);
         const float NEG_INF = -__int_as_float(0x7f800000);
-        float m_used = NEG_INF, l = 0.0f;
+        const float c2 = args.scale_log2;
+        float m_used = NEG_INF, l = 0.0f;  // m_used in base-2 units of the scaled scores
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
             const int st = j & 1;
+            const uint32_t xb = static_cast<uint32_t>(j & 1) * (2 * 128 * 4);
             if (!warp_wait(b_sf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1006, j)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[C::BKV];
+            float x[64];
             {
-                uint32_t u[32];
+                uint32_t u0[32], u1[32];
+                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
+                tmem_ld_32x32b_x32(t_lane + 128u * st + cb + 32u, u1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < C::BKV / 32; ++c) {
-                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(u[i]) * args.scale_log2;
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = __uint_as_float(u0[i]);
+                    x[32 + i] = __uint_as_float(u1[i]);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_sfree + 8 * st);
-            const int k0 = j * C::BKV;
-            if ((args.causal && k0 + C::BKV - 1 > q0) || k0 + C::BKV > s) {  // CTA-uniform
+            const int k0 = j * C::BKV + cb;
+            if ((args.causal && j * C::BKV + C::BKV - 1 > q0) || j * C::BKV + C::BKV > s) {  // CTA-uniform
 #pragma unroll
-                for (int c = 0; c < C::BKV; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     const int key = k0 + c;
                     if (key >= s || (args.causal && key > qi)) x[c] = NEG_INF;
                 }
             }
-            float mx = x[0];
-#pragma unroll
-            for (int c = 1; c < C::BKV; ++c) mx = fmaxf(mx, x[c]);
+            sts_f32(x_mine + xb, max_tree(x));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pair + 8 * (2 * q + (j & 1)));
+            if (!warp_wait(b_pair + 8 * (2 * q + (j & 1)), (j >> 1) & 1, abort_flag, args.status, limit,
+                           DEV_TIMEOUT_EPILOGUE, 1010, j)) {
+                ok = false;
+                break;
+            }
+            const float mx = fmaxf(lds_f32(x_mine + xb), lds_f32(x_peer + xb)) * c2;  // scale > 0: commutes
             const bool resc = mx > m_used + static_cast<float>(kLazyRescaleLog2);
             float alpha = 1.0f;
             if (resc) {
@@ -327,59 +406,57 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
                 m_used = mx;
                 l *= alpha;
             }
-            const float mref = (m_used == NEG_INF) ? 0.0f : m_used;
-            float rs = 0.0f;
+            const float nref = (m_used == NEG_INF) ? 0.0f : -m_used;
 #pragma unroll
-            for (int c = 0; c < C::BKV; ++c) {
-                x[c] = ex2(x[c] - mref);
-                rs += x[c];
-            }
-            l += rs;
-            // the P buffer is free once PV_{j-2} has completed
-            if (j >= 2 && !warp_wait(b_pv + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                     DEV_TIMEOUT_EPILOGUE, 1007, j)) {
-                ok = false;
-                break;
-            }
-            if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-                // O holds PV_0..PV_{j-1} once PV_{j-1} has completed: rescale it in place
-                if (!warp_wait(b_pv + 8 * (st ^ 1), ((j - 1) >> 1) & 1, abort_flag, args.status, limit,
-                               DEV_TIMEOUT_EPILOGUE, 1008, j)) {
+            for (int c = 0; c < 64; ++c) x[c] = ex2(fmaf(x[c], c2, nref));
+            l += sum_tree(x);
+            // P (single buffer) and O are free to touch once PV_{j-1} has completed
+            if (j >= 1) {
+                if (!warp_wait(b_pv, (j - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1007, j)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                uint32_t o[32];
+                if (__any_sync(0xffffffffu, resc)) {  // rescale this half of the O row in place
+                    tc_fence_after();
+                    uint32_t o[32];
 #pragma unroll 1
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    tmem_ld_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
-                    tmem_ld_wait();
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t ta = t_lane + C::O_COL + cb + 32u * c;
+                        tmem_ld_32x32b_x32(ta, o);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st_32x32b_x32(ta, o);
+                    }
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
             }
-            store_row_sw128<C::BKV, C::BQ>(sP + st * C::TILE, r, x);
+            store_row_part_sw128<64, C::BQ>(sP, r, cb, x);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_pf + 8 * st);
+            if (lane == 0) mbar_arrive(b_pf);
         }
         if (ok && nkb > 0 &&
-            warp_wait(b_pv + 8 * ((nkb - 1) & 1), ((nkb - 1) >> 1) & 1, abort_flag, args.status, limit,
-                      DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
+            warp_wait(b_pv, (nkb - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
             tc_fence_after();
-            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ;
+            const uint32_t xb = static_cast<uint32_t>(nkb & 1) * (2 * 128 * 4);
+            sts_f32(x_mine + xb, l);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pair + 8 * (2 * q + (nkb & 1)));
+            const bool paired = warp_wait(b_pair + 8 * (2 * q + (nkb & 1)), (nkb >> 1) & 1, abort_flag, args.status,
+                                          limit, DEV_TIMEOUT_EPILOGUE, 1011, nkb);
+            const float lt = l + lds_f32(x_peer + xb);  // both halves used the same references
+            const float inv_l = lt > 0.0f ? 1.0f / lt : 0.0f;
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ + cb;
             uint32_t o[32];
 #pragma unroll 1
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::O_COL + cb + 32u * c, o);
                 tmem_ld_wait();
-                if (qi < s) store32_global(dst + 32 * c, o, inv_l);
+                if (paired && qi < s) store32_global(dst + 32 * c, o, inv_l);
             }
-            if (qi < s) args.lse[static_cast<size_t>(bh) * s + qi] = m_used + log2f(l);
+            if (paired && half == 0 && qi < s) args.lse[static_cast<size_t>(bh) * s + qi] = m_used + log2f(lt);
         }
     }
 
@@ -393,14 +470,15 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
 
 struct DkdvCfg {
     static constexpr int BKV = 128, BQ = 64;
+    static constexpr int THREADS = 320;  // producer, MMA, 8 element-wise warps (two threads per key)
+    static constexpr int STAGES = 3;                    // Q / dC blocks in flight
     static constexpr uint32_t KT = 128 * kHeadDim * 2;  // K or V block: 32 KB
     static constexpr uint32_t QT = 64 * kHeadDim * 2;   // Q or dC block: 16 KB
     static constexpr uint32_t PT = 128 * 64 * 2;        // P^T or dS^T block: 16 KB
-    static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_Q = 2 * KT, OFF_DO = 2 * KT + 2 * QT,
-                              OFF_P = 2 * KT + 4 * QT, OFF_DS = OFF_P + 2 * PT, OFF_LD = OFF_DS + 2 * PT,
-                              OFF_BAR = OFF_LD + 4 * 2 * 64 * 4;
-    // barriers: kv | qdofull[2] | qdoempty[2] | stfull[2] | stfree[2] | pdfull[2] | accfull | drain
-    static constexpr int NUM_BARS = 13;
+    static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_QD = 2 * KT, OFF_P = 2 * KT + STAGES * 2 * QT,
+                              OFF_DS = OFF_P + PT, OFF_LD = OFF_DS + PT, OFF_BAR = OFF_LD + 8 * 2 * 32 * 4;
+    // barriers: kv | qdofull[3] | qdoempty[3] | stfull[2] | stfree[2] | pdfull | pdfree | accfull | drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 4 + 4;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, 128, false, true);
@@ -409,25 +487,29 @@ struct DkdvCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = DkdvCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q, sdO = base + C::OFF_DO,
-                   sP = base + C::OFF_P, sdS = base + C::OFF_DS, sLD = base + C::OFF_LD;
+    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQD = base + C::OFF_QD, sP = base + C::OFF_P,
+                   sdS = base + C::OFF_DS, sLD = base + C::OFF_LD;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_kv = bar, b_qf = bar + 8, b_qe = bar + 24, b_stf = bar + 40, b_stfree = bar + 56,
-                   b_pdf = bar + 72, b_acc = bar + 88, b_drain = bar + 96;
+    const uint32_t b_kv = bar, b_qf = bar + 8, b_qe = b_qf + 8 * C::STAGES, b_stf = b_qe + 8 * C::STAGES,
+                   b_stfree = b_stf + 16, b_pdf = b_stfree + 16, b_pdfree = b_pdf + 8, b_acc = b_pdfree + 8,
+                   b_drain = b_acc + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = args.s, a = args.a;
-    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
-    const int kb = static_cast<int>(blockIdx.y);  // with a causal mask, low key blocks have the most queries
+    // Head-major order (the key blocks of one head share its Q and dC blocks through L2);
+    // with a causal mask, low key blocks have the most queries and start first.
+    const int nkbk = (s + C::BKV - 1) / C::BKV;
+    const int bh = static_cast<int>(blockIdx.x) / nkbk, bi = bh / a, head = bh % a;
+    const int kb = static_cast<int>(blockIdx.x) % nkbk;
     const int k0 = kb * C::BKV;
     const int nqb_all = (s + C::BQ - 1) / C::BQ;
     const int qb_first = args.causal ? k0 / C::BQ : 0;
@@ -439,13 +521,16 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(b_qf + 8 * i, 1);
             mbar_init(b_qe + 8 * i, 1);
-            mbar_init(b_stf + 8 * i, 1);
-            mbar_init(b_stfree + 8 * i, 4);
-            mbar_init(b_pdf + 8 * i, 4);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_stf + 8 * i, 1);
+            mbar_init(b_stfree + 8 * i, 8);
+        }
+        mbar_init(b_pdf, 8);
+        mbar_init(b_pdfree, 1);
         mbar_init(b_acc, 1);
         mbar_init(b_drain, 1);
         *abort_flag = 0;
@@ -465,7 +550,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
 
     if (warp == 0) {
         if (lane == 0) {
-            // drain indices: 0 = kv, 1..2 = qdofull
+            // drain indices: 0 = kv, 1 + i = qdofull[i]
             uint32_t issued = 1u, par = 0u;
             bool ok = true;
             mbar_arrive_expect_tx(b_kv, 2 * C::KT);
@@ -474,31 +559,33 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
             tma_load_2d(sV, &args.tmKV, colV, row0 + k0, b_kv);
             tma_load_2d(sV + C::KT / 2, &args.tmKV, colV + 64, row0 + k0, b_kv);
             for (int i = 0; i < nq; ++i) {
-                const int st = i & 1;
-                if (i >= 2 && !mbar_wait_bounded(b_qe + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                                 DEV_TIMEOUT_PRODUCER, 3000, i)) {
+                const int st = i % C::STAGES;
+                const uint32_t ph = static_cast<uint32_t>(i / C::STAGES) & 1u;
+                if (i >= C::STAGES && !mbar_wait_bounded(b_qe + 8 * st, ph ^ 1u, abort_flag, args.status, limit,
+                                                         DEV_TIMEOUT_PRODUCER, 3000, i)) {
                     ok = false;
                     break;
                 }
                 const int y = row0 + (qb_first + i) * C::BQ;
-                mbar_arrive_expect_tx(b_qf + 8 * st, 2 * C::QT);
-                tma_load_2d(sQ + st * C::QT, &args.tmQ, colQ, y, b_qf + 8 * st);
-                tma_load_2d(sQ + st * C::QT + C::QT / 2, &args.tmQ, colQ + 64, y, b_qf + 8 * st);
-                tma_load_2d(sdO + st * C::QT, &args.tmdO, colQ, y, b_qf + 8 * st);
-                tma_load_2d(sdO + st * C::QT + C::QT / 2, &args.tmdO, colQ + 64, y, b_qf + 8 * st);
+                const uint32_t dq = sQD + st * 2 * C::QT, dd = dq + C::QT, fb = b_qf + 8 * st;
+                mbar_arrive_expect_tx(fb, 2 * C::QT);
+                tma_load_2d(dq, &args.tmQ, colQ, y, fb);
+                tma_load_2d(dq + C::QT / 2, &args.tmQ, colQ + 64, y, fb);
+                tma_load_2d(dd, &args.tmdO, colQ, y, fb);
+                tma_load_2d(dd + C::QT / 2, &args.tmdO, colQ + 64, y, fb);
                 issued |= 1u << (1 + st);
-                par = (par & ~(1u << (1 + st))) | (static_cast<uint32_t>((i >> 1) & 1) << (1 + st));
+                par = (par & ~(1u << (1 + st))) | (ph << (1 + st));
             }
-            if (!ok) drain_loads(bar, 3, issued, par, args.status);
+            if (!ok) drain_loads(bar, 1 + C::STAGES, issued, par, args.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_kv, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 3001, -1);
             bool any = false;
             for (int i = 0; ok && i <= nq; ++i) {
-                if (i < nq) {
-                    const int st = i & 1;
-                    if (!mbar_wait_bounded(b_qf + 8 * st, (i >> 1) & 1, abort_flag, args.status, limit,
+                if (i < nq) {  // S^T_i = K Q_i^T, dP^T_i = V dC_i^T
+                    const int st = i & 1, qs = i % C::STAGES;
+                    if (!mbar_wait_bounded(b_qf + 8 * qs, (i / C::STAGES) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 3002, i) ||
                         (i >= 2 && !mbar_wait_bounded(b_stfree + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status,
                                                       limit, DEV_TIMEOUT_MMA_ACC, 3003, i))) {
@@ -506,7 +593,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qbuf = sQ + st * C::QT, dobuf = sdO + st * C::QT;
+                    const uint32_t qbuf = sQD + qs * 2 * C::QT, dobuf = qbuf + C::QT;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t ka = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
@@ -517,51 +604,52 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     any = true;
                     umma_commit(b_stf + 8 * st);
                 }
-                if (i >= 1) {
-                    const int pi = i - 1, pst = pi & 1;
-                    if (!mbar_wait_bounded(b_pdf + 8 * pst, (pi >> 1) & 1, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_ACC, 3004, pi)) {
+                if (i >= 1) {  // dV += P^T_{i-1} dC_{i-1}, dK += dS^T_{i-1} Q_{i-1}
+                    const int pi = i - 1, qs = pi % C::STAGES;
+                    if (!mbar_wait_bounded(b_pdf, pi & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 3004,
+                                           pi)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qbuf = sQ + pst * C::QT, dobuf = sdO + pst * C::QT;
-                    const uint32_t pbuf = sP + pst * C::PT, dsbuf = sdS + pst * C::PT;
+                    const uint32_t qbuf = sQD + qs * 2 * C::QT, dobuf = qbuf + C::QT;
 #pragma unroll
                     for (int k = 0; k < C::BQ / 16; ++k) {
                         const uint32_t acc = (pi > 0 || k > 0) ? 1u : 0u;
-                        umma_bf16(tmem + C::DV_COL, desc_k(pbuf + 32u * k), desc_mn(dobuf + 2048u * k, C::QT / 2),
+                        umma_bf16(tmem + C::DV_COL, desc_k(sP + 32u * k), desc_mn(dobuf + 2048u * k, C::QT / 2),
                                   C::IDESC_ACC, acc);
-                        umma_bf16(tmem + C::DK_COL, desc_k(dsbuf + 32u * k), desc_mn(qbuf + 2048u * k, C::QT / 2),
+                        umma_bf16(tmem + C::DK_COL, desc_k(sdS + 32u * k), desc_mn(qbuf + 2048u * k, C::QT / 2),
                                   C::IDESC_ACC, acc);
                     }
-                    umma_commit(b_qe + 8 * pst);
+                    umma_commit(b_qe + 8 * qs);
+                    umma_commit(b_pdfree);
                 }
             }
             if (ok && any) umma_commit(b_acc);
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
-        const int q = warp & 3;
+        // Two threads per key row: warp w (2..9) takes TMEM lane quadrant w % 4 and query
+        // columns [32 half, 32 half + 32) of each 64-query block, half = (w - 2) / 4.
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int kj = k0 + r;
+        const int cb = 32 * half;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        const uint32_t sL = sLD + static_cast<uint32_t>(q) * 512u, sD = sL + 256u;
+        const uint32_t sL = sLD + static_cast<uint32_t>(warp - 2) * 256u, sD = sL + 128u;
         const size_t lbase = static_cast<size_t>(bh) * s;
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int st = i & 1;
-            const int qq0 = (qb_first + i) * C::BQ;
-            // this block's L and D into the warp's own staging slots
+            const int qq0 = (qb_first + i) * C::BQ + cb;  // this thread's first query column
+            // this warp's 32 values of L and D into its own staging slots
             {
-                const int qa = qq0 + lane, qb2 = qq0 + 32 + lane;
-                const float la = qa < s ? args.lse[lbase + qa] : 0.0f, lb = qb2 < s ? args.lse[lbase + qb2] : 0.0f;
-                const float da = qa < s ? args.delta[lbase + qa] : 0.0f, db = qb2 < s ? args.delta[lbase + qb2] : 0.0f;
+                const int qa = qq0 + lane;
+                const float la = qa < s ? args.lse[lbase + qa] : 0.0f;
+                const float da = qa < s ? args.delta[lbase + qa] : 0.0f;
                 __syncwarp();
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sL + 4u * lane), "f"(la) : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sL + 128u + 4u * lane), "f"(lb) : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sD + 4u * lane), "f"(da) : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sD + 128u + 4u * lane), "f"(db) : "memory");
+                sts_f32(sL + 4u * lane, la);
+                sts_f32(sD + 4u * lane, da);
                 __syncwarp();
             }
             if (!warp_wait(b_stf + 8 * st, (i >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3005, i)) {
@@ -569,27 +657,25 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            float p[C::BQ], dp[C::BQ];
+            float p[32], dp[32];
             {
-                uint32_t u[32];
+                uint32_t u0[32], u1[32];
+                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
+                tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + cb, u1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < C::BQ / 32; ++c) {
-                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) p[32 * c + e] = __uint_as_float(u[e]);
-                    tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) dp[32 * c + e] = __uint_as_float(u[e]);
+                for (int e = 0; e < 32; ++e) {
+                    p[e] = __uint_as_float(u0[e]);
+                    dp[e] = __uint_as_float(u1[e]);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_stfree + 8 * st);
-            const bool need_mask = (args.causal && qq0 < k0 + C::BKV - 1) || qq0 + C::BQ > s || k0 + C::BKV > s;
+            const int blk0 = (qb_first + i) * C::BQ;
+            const bool need_mask = (args.causal && blk0 < k0 + C::BKV - 1) || blk0 + C::BQ > s || k0 + C::BKV > s;
 #pragma unroll
-            for (int c4 = 0; c4 < C::BQ / 4; ++c4) {
+            for (int c4 = 0; c4 < 8; ++c4) {
                 const float4 L4 = lds128f(sL + 16u * c4), D4 = lds128f(sD + 16u * c4);
                 const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
 #pragma unroll
@@ -604,31 +690,32 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     dp[c] = pv * (dp[c] - Dv[e]);
                 }
             }
-            // P^T and dS^T buffers are free once the dV / dK MMAs of block i-2 completed
-            if (i >= 2 && !warp_wait(b_qe + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                     DEV_TIMEOUT_EPILOGUE, 3006, i)) {
+            // the single P^T / dS^T buffer is free once the dV / dK MMAs of block i-1 completed
+            if (i >= 1 && !warp_wait(b_pdfree, (i - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE,
+                                     3006, i)) {
                 ok = false;
                 break;
             }
-            store_row_sw128<C::BQ, C::BKV>(sP + st * C::PT, r, p);
-            store_row_sw128<C::BQ, C::BKV>(sdS + st * C::PT, r, dp);
+            store_row_part_sw128<32, C::BKV>(sP, r, cb, p);
+            store_row_part_sw128<32, C::BKV>(sdS, r, cb, dp);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_pdf + 8 * st);
+            if (lane == 0) mbar_arrive(b_pdf);
         }
         if (ok && nq > 0 && warp_wait(b_acc, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3007, -1)) {
             tc_fence_after();
             __nv_bfloat16* rowp = args.out + static_cast<size_t>(row0 + kj) * (3 * hd);
+            const int db = 64 * half;  // this thread's half of the d columns of dV and dK
             uint32_t o[32];
 #pragma unroll 1
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::DV_COL + 32u * c, o);
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::DV_COL + db + 32u * c, o);
                 tmem_ld_wait();
-                if (kj < s) store32_global(rowp + colV + 32 * c, o, 1.0f);
-                tmem_ld_32x32b_x32(t_lane + C::DK_COL + 32u * c, o);
+                if (kj < s) store32_global(rowp + colV + db + 32 * c, o, 1.0f);
+                tmem_ld_32x32b_x32(t_lane + C::DK_COL + db + 32u * c, o);
                 tmem_ld_wait();
-                if (kj < s) store32_global(rowp + colK + 32 * c, o, args.scale);
+                if (kj < s) store32_global(rowp + colK + db + 32 * c, o, args.scale);
             }
         }
     }
@@ -643,13 +730,15 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dkdv_kernel(const __grid_cons
 
 struct DqCfg {
     static constexpr int BQ = 128, BKV = 64;
+    static constexpr int THREADS = 320;  // producer, MMA, 8 element-wise warps (two threads per query)
+    static constexpr int STAGES = 4;                    // K / V blocks in flight
     static constexpr uint32_t QT = 128 * kHeadDim * 2;  // Q or dC block: 32 KB
     static constexpr uint32_t KT = 64 * kHeadDim * 2;   // K or V block: 16 KB
     static constexpr uint32_t ST = 128 * 64 * 2;        // dS block: 16 KB
-    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_K = 2 * QT, OFF_V = 2 * QT + 2 * KT,
-                              OFF_DS = 2 * QT + 4 * KT, OFF_BAR = OFF_DS + 2 * ST;
-    // barriers: qdo | kvfull[2] | kvempty[2] | spfull[2] | spfree[2] | dsfull[2] | dqfull | drain
-    static constexpr int NUM_BARS = 13;
+    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_KV = 2 * QT, OFF_DS = 2 * QT + STAGES * 2 * KT,
+                              OFF_BAR = OFF_DS + 2 * ST;
+    // barriers: qdo | kvfull[4] | kvempty[4] | spfull[2] | spfree[2] | dsfull[2] | dsfree[2] | dqfull | drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 8 + 2;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 128, false, true);
@@ -658,25 +747,27 @@ struct DqCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = DqCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sK = base + C::OFF_K, sV = base + C::OFF_V,
-                   sdS = base + C::OFF_DS;
+    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sKV = base + C::OFF_KV, sdS = base + C::OFF_DS;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_qdo = bar, b_kvf = bar + 8, b_kve = bar + 24, b_spf = bar + 40, b_spfree = bar + 56,
-                   b_dsf = bar + 72, b_dq = bar + 88, b_drain = bar + 96;
+    const uint32_t b_qdo = bar, b_kvf = bar + 8, b_kve = b_kvf + 8 * C::STAGES, b_spf = b_kve + 8 * C::STAGES,
+                   b_spfree = b_spf + 16, b_dsf = b_spfree + 16, b_dsfree = b_dsf + 16, b_dq = b_dsfree + 16,
+                   b_drain = b_dq + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int s = args.s, a = args.a;
-    const int bh = blockIdx.x, bi = bh / a, head = bh % a;
-    const int qb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest rows first
+    // Head-major order, longest rows first within a head (as in the forward kernel).
+    const int nqb = (s + C::BQ - 1) / C::BQ;
+    const int bh = static_cast<int>(blockIdx.x) / nqb, bi = bh / a, head = bh % a;
+    const int qb = nqb - 1 - static_cast<int>(blockIdx.x) % nqb;
     const int q0 = qb * C::BQ;
     const int nkb_all = (s + C::BKV - 1) / C::BKV;
     const int nkb = args.causal ? min(nkb_all, (q0 + C::BQ - 1) / C::BKV + 1) : nkb_all;
@@ -687,12 +778,15 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         mbar_init(b_qdo, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(b_kvf + 8 * i, 1);
             mbar_init(b_kve + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(b_spf + 8 * i, 1);
-            mbar_init(b_spfree + 8 * i, 4);
-            mbar_init(b_dsf + 8 * i, 4);
+            mbar_init(b_spfree + 8 * i, 8);
+            mbar_init(b_dsf + 8 * i, 8);
+            mbar_init(b_dsfree + 8 * i, 1);
         }
         mbar_init(b_dq, 1);
         mbar_init(b_drain, 1);
@@ -713,7 +807,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t issued = 1u, par = 0u;  // drain indices: 0 = qdo, 1..2 = kvfull
+            uint32_t issued = 1u, par = 0u;  // drain indices: 0 = qdo, 1 + i = kvfull[i]
             bool ok = true;
             mbar_arrive_expect_tx(b_qdo, 2 * C::QT);
             tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_qdo);
@@ -721,31 +815,33 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
             tma_load_2d(sdO, &args.tmdO, colQ, row0 + q0, b_qdo);
             tma_load_2d(sdO + C::QT / 2, &args.tmdO, colQ + 64, row0 + q0, b_qdo);
             for (int j = 0; j < nkb; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait_bounded(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                                 DEV_TIMEOUT_PRODUCER, 2000, j)) {
+                const int st = j % C::STAGES;
+                const uint32_t ph = static_cast<uint32_t>(j / C::STAGES) & 1u;
+                if (j >= C::STAGES && !mbar_wait_bounded(b_kve + 8 * st, ph ^ 1u, abort_flag, args.status, limit,
+                                                         DEV_TIMEOUT_PRODUCER, 2000, j)) {
                     ok = false;
                     break;
                 }
                 const int y = row0 + j * C::BKV;
-                mbar_arrive_expect_tx(b_kvf + 8 * st, 2 * C::KT);
-                tma_load_2d(sK + st * C::KT, &args.tmKV, colK, y, b_kvf + 8 * st);
-                tma_load_2d(sK + st * C::KT + C::KT / 2, &args.tmKV, colK + 64, y, b_kvf + 8 * st);
-                tma_load_2d(sV + st * C::KT, &args.tmKV, colV, y, b_kvf + 8 * st);
-                tma_load_2d(sV + st * C::KT + C::KT / 2, &args.tmKV, colV + 64, y, b_kvf + 8 * st);
+                const uint32_t dk = sKV + st * 2 * C::KT, dv = dk + C::KT, fb = b_kvf + 8 * st;
+                mbar_arrive_expect_tx(fb, 2 * C::KT);
+                tma_load_2d(dk, &args.tmKV, colK, y, fb);
+                tma_load_2d(dk + C::KT / 2, &args.tmKV, colK + 64, y, fb);
+                tma_load_2d(dv, &args.tmKV, colV, y, fb);
+                tma_load_2d(dv + C::KT / 2, &args.tmKV, colV + 64, y, fb);
                 issued |= 1u << (1 + st);
-                par = (par & ~(1u << (1 + st))) | (static_cast<uint32_t>((j >> 1) & 1) << (1 + st));
+                par = (par & ~(1u << (1 + st))) | (ph << (1 + st));
             }
-            if (!ok) drain_loads(bar, 3, issued, par, args.status);
+            if (!ok) drain_loads(bar, 1 + C::STAGES, issued, par, args.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_qdo, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 2001, -1);
             bool any = false;
             for (int j = 0; ok && j <= nkb; ++j) {
-                if (j < nkb) {
-                    const int st = j & 1;
-                    if (!mbar_wait_bounded(b_kvf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
+                if (j < nkb) {  // S_j = Q K_j^T, dP_j = dC V_j^T
+                    const int st = j & 1, ks = j % C::STAGES;
+                    if (!mbar_wait_bounded(b_kvf + 8 * ks, (j / C::STAGES) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 2002, j) ||
                         (j >= 2 && !mbar_wait_bounded(b_spfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
                                                       limit, DEV_TIMEOUT_MMA_ACC, 2003, j))) {
@@ -753,7 +849,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbuf = sK + st * C::KT, vbuf = sV + st * C::KT;
+                    const uint32_t kbuf = sKV + ks * 2 * C::KT, vbuf = kbuf + C::KT;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t aq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
@@ -764,32 +860,36 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
                     any = true;
                     umma_commit(b_spf + 8 * st);
                 }
-                if (j >= 1) {
-                    const int pj = j - 1, pst = pj & 1;
+                if (j >= 1) {  // dQ += dS_{j-1} K_{j-1}
+                    const int pj = j - 1, pst = pj & 1, ks = pj % C::STAGES;
                     if (!mbar_wait_bounded(b_dsf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_ACC, 2004, pj)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dsbuf = sdS + pst * C::ST, kbuf = sK + pst * C::KT;
+                    const uint32_t dsbuf = sdS + pst * C::ST, kbuf = sKV + ks * 2 * C::KT;
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k)
                         umma_bf16(tmem + C::DQ_COL, desc_k(dsbuf + 32u * k), desc_mn(kbuf + 2048u * k, C::KT / 2),
                                   C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(b_kve + 8 * pst);
+                    umma_commit(b_kve + 8 * ks);
+                    umma_commit(b_dsfree + 8 * pst);
                 }
             }
             if (ok && any) umma_commit(b_dq);
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
-        const int q = warp & 3;
+        // Two threads per query row: warp w (2..9) takes TMEM lane quadrant w % 4 and key
+        // columns [32 half, 32 half + 32) of each 64-key block, half = (w - 2) / 4.
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int qi = q0 + r;
+        const int cb = 32 * half;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const size_t li = static_cast<size_t>(bh) * s + qi;
-        const float Lq = qi < s ? args.lse[li] : 0.0f;
+        const float nLq = qi < s ? -args.lse[li] : 0.0f;
         const float Dq = qi < s ? args.delta[li] : 0.0f;
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
@@ -799,19 +899,16 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
                 break;
             }
             tc_fence_after();
-            float p[C::BKV], dp[C::BKV];
+            float p[32], dp[32];
             {
-                uint32_t u[32];
+                uint32_t u0[32], u1[32];
+                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
+                tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + cb, u1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < C::BKV / 32; ++c) {
-                    tmem_ld_32x32b_x32(t_lane + 128u * st + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) p[32 * c + e] = __uint_as_float(u[e]);
-                    tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) dp[32 * c + e] = __uint_as_float(u[e]);
+                for (int e = 0; e < 32; ++e) {
+                    p[e] = __uint_as_float(u0[e]);
+                    dp[e] = __uint_as_float(u1[e]);
                 }
             }
             tc_fence_before();
@@ -820,20 +917,21 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
 #pragma unroll
-            for (int c = 0; c < C::BKV; ++c) {
-                float pv = ex2(fmaf(p[c], args.scale_log2, -Lq));
+            for (int c = 0; c < 32; ++c) {
+                float pv = ex2(fmaf(p[c], args.scale_log2, nLq));
                 if (need_mask) {
-                    const int key = kk0 + c;
+                    const int key = kk0 + cb + c;
                     if (qi >= s || key >= s || (args.causal && key > qi)) pv = 0.0f;
                 }
                 dp[c] = pv * (dp[c] - Dq);
             }
-            if (j >= 2 && !warp_wait(b_kve + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+            // the dS buffer is free once dQ_{j-2} has completed
+            if (j >= 2 && !warp_wait(b_dsfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
                                      DEV_TIMEOUT_EPILOGUE, 2006, j)) {
                 ok = false;
                 break;
             }
-            store_row_sw128<C::BKV, C::BQ>(sdS + st * C::ST, r, dp);
+            store_row_part_sw128<32, C::BQ>(sdS + st * C::ST, r, cb, dp);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -841,11 +939,12 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         if (ok && nkb > 0 && warp_wait(b_dq, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2007, -1)) {
             tc_fence_after();
-            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * (3 * hd) + colQ;
+            const int db = 64 * half;  // this thread's half of the d columns
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * (3 * hd) + colQ + db;
             uint32_t o[32];
 #pragma unroll 1
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::DQ_COL + 32u * c, o);
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::DQ_COL + db + 32u * c, o);
                 tmem_ld_wait();
                 if (qi < s) store32_global(dst + 32 * c, o, args.scale);
             }
@@ -895,8 +994,10 @@ cudaError_t launch_tile_kernel(K kern, const AttnArgs& args, int blocks_y, cudaS
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    if (blocks_y <= 0 || args.b * args.a <= 0) return cudaSuccess;
-    kern<<<dim3(args.b * args.a, blocks_y), 192, Cfg::SMEM_BYTES, stream>>>(args);
+    const long long grid = static_cast<long long>(args.b) * args.a * blocks_y;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(grid), Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(args);
     return cudaGetLastError();
 }
 
