@@ -130,6 +130,13 @@ __device__ __forceinline__ void store32_global(__nv_bfloat16* dst, const uint32_
 }
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc_sw128(addr, 16u, 1024u); }
+
+// The descriptor of a tile `off` bytes further on: the start-address field (bits 0-13) holds
+// addr >> 4 and every shared address here is below 2^18, so the field never carries and a
+// 64-bit add equals a fresh encoding. Building each buffer's descriptor once and adding
+// constants keeps the MMA-issuing thread to a few instructions per MMA (it shares its
+// SM sub-partition with two busy softmax warps, and the MMAs here are short).
+__device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t off) { return base_desc + (off >> 4); }
 __device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t chunk_stride)
 {
     return smem_desc_sw128(addr, chunk_stride, 1024u);
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_q, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 1001, -1);
             bool any = false;
+            const uint64_t dQ = desc_k(sQ), dKV = desc_k(sKV), dP = desc_k(sP), dV = desc_mn(sKV, C::TILE / 2);
             for (int j = 0; ok && j <= nkb; ++j) {
                 if (j < nkb) {  // S_j = Q K_j^T
                     const int st = j & 1, n = 2 * j, slot = n % C::SLOTS;
@@ -308,11 +316,11 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbuf = sKV + slot * C::TILE;
+                    const uint64_t dK = desc_at(dKV, slot * C::TILE);
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t off = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + 128u * st, desc_k(sQ + off), desc_k(kbuf + off), C::IDESC_S, k > 0);
+                        umma_bf16(tmem + 128u * st, desc_at(dQ, off), desc_at(dK, off), C::IDESC_S, k > 0);
                     }
                     any = true;
                     umma_commit(b_sf + 8 * st);
@@ -328,12 +336,12 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t vbuf = sKV + slot * C::TILE;
+                    const uint64_t dVs = desc_at(dV, slot * C::TILE);
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k) {
                         const uint32_t aoff = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + C::O_COL, desc_k(sP + aoff), desc_mn(vbuf + 2048u * k, C::TILE / 2),
-                                  C::IDESC_PV, (pj > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16(tmem + C::O_COL, desc_at(dP, aoff), desc_at(dVs, 2048u * k), C::IDESC_PV,
+                                  (pj > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(b_pv);
                     umma_commit(b_empty + 8 * slot);
@@ -582,6 +590,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_kv, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 3001, -1);
             bool any = false;
+            const uint64_t dK = desc_k(sK), dV = desc_k(sV), dQD = desc_k(sQD), dQDmn = desc_mn(sQD, C::QT / 2),
+                           dP = desc_k(sP), dS = desc_k(sdS);
             for (int i = 0; ok && i <= nq; ++i) {
                 if (i < nq) {  // S^T_i = K Q_i^T, dP^T_i = V dC_i^T
                     const int st = i & 1, qs = i % C::STAGES;
@@ -593,13 +603,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qbuf = sQD + qs * 2 * C::QT, dobuf = qbuf + C::QT;
+                    const uint32_t qoff = qs * 2 * C::QT, dooff = qoff + C::QT;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t ka = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
                         const uint32_t kq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + 128u * st, desc_k(sK + ka), desc_k(qbuf + kq), C::IDESC_ST, k > 0);
-                        umma_bf16(tmem + 128u * st + 64u, desc_k(sV + ka), desc_k(dobuf + kq), C::IDESC_ST, k > 0);
+                        umma_bf16(tmem + 128u * st, desc_at(dK, ka), desc_at(dQD, qoff + kq), C::IDESC_ST, k > 0);
+                        umma_bf16(tmem + 128u * st + 64u, desc_at(dV, ka), desc_at(dQD, dooff + kq), C::IDESC_ST,
+                                  k > 0);
                     }
                     any = true;
                     umma_commit(b_stf + 8 * st);
@@ -612,14 +623,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qbuf = sQD + qs * 2 * C::QT, dobuf = qbuf + C::QT;
+                    const uint32_t qoff = qs * 2 * C::QT, dooff = qoff + C::QT;
 #pragma unroll
                     for (int k = 0; k < C::BQ / 16; ++k) {
                         const uint32_t acc = (pi > 0 || k > 0) ? 1u : 0u;
-                        umma_bf16(tmem + C::DV_COL, desc_k(sP + 32u * k), desc_mn(dobuf + 2048u * k, C::QT / 2),
-                                  C::IDESC_ACC, acc);
-                        umma_bf16(tmem + C::DK_COL, desc_k(sdS + 32u * k), desc_mn(qbuf + 2048u * k, C::QT / 2),
-                                  C::IDESC_ACC, acc);
+                        umma_bf16(tmem + C::DV_COL, desc_at(dP, 32u * k), desc_at(dQDmn, dooff + 2048u * k), C::IDESC_ACC,
+                                  acc);
+                        umma_bf16(tmem + C::DK_COL, desc_at(dS, 32u * k), desc_at(dQDmn, qoff + 2048u * k), C::IDESC_ACC,
+                                  acc);
                     }
                     umma_commit(b_qe + 8 * qs);
                     umma_commit(b_pdfree);
@@ -838,6 +849,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_qdo, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 2001, -1);
             bool any = false;
+            const uint64_t dQ = desc_k(sQ), dO = desc_k(sdO), dKV = desc_k(sKV), dKmn = desc_mn(sKV, C::KT / 2),
+                           dS = desc_k(sdS);
             for (int j = 0; ok && j <= nkb; ++j) {
                 if (j < nkb) {  // S_j = Q K_j^T, dP_j = dC V_j^T
                     const int st = j & 1, ks = j % C::STAGES;
@@ -849,13 +862,13 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbuf = sKV + ks * 2 * C::KT, vbuf = kbuf + C::KT;
+                    const uint32_t koff = ks * 2 * C::KT, voff = koff + C::KT;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t aq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
                         const uint32_t bk = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + 128u * st, desc_k(sQ + aq), desc_k(kbuf + bk), C::IDESC_S, k > 0);
-                        umma_bf16(tmem + 128u * st + 64u, desc_k(sdO + aq), desc_k(vbuf + bk), C::IDESC_S, k > 0);
+                        umma_bf16(tmem + 128u * st, desc_at(dQ, aq), desc_at(dKV, koff + bk), C::IDESC_S, k > 0);
+                        umma_bf16(tmem + 128u * st + 64u, desc_at(dO, aq), desc_at(dKV, voff + bk), C::IDESC_S, k > 0);
                     }
                     any = true;
                     umma_commit(b_spf + 8 * st);
@@ -868,10 +881,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dsbuf = sdS + pst * C::ST, kbuf = sKV + ks * 2 * C::KT;
+                    const uint32_t dsoff = pst * C::ST, koff = ks * 2 * C::KT;
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k)
-                        umma_bf16(tmem + C::DQ_COL, desc_k(dsbuf + 32u * k), desc_mn(kbuf + 2048u * k, C::KT / 2),
+                        umma_bf16(tmem + C::DQ_COL, desc_at(dS, dsoff + 32u * k), desc_at(dKmn, koff + 2048u * k),
                                   C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
                     umma_commit(b_kve + 8 * ks);
                     umma_commit(b_dsfree + 8 * pst);
