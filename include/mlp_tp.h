@@ -155,6 +155,22 @@ size_t mlp_tp_swiglu_workspace_bytes(int T, int h, int f, int t);
 /* Device bytes mlp_tp_backward needs as workspace for these sizes (0 on invalid sizes). */
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
 
+/* GELU recompute ("Efficient Large-Scale Language Model Training ... Megatron-LM", section 3
+ * "Activation Recomputation": keep fewer activations, recompute them in the backward). The
+ * backward of the block when the forward's G was not kept: the caller may pass the forward
+ * any scratch buffer for G (one shared by every layer) and keep only H. The dH GEMM's
+ * epilogue recomputes G = GELU(H) from the stored bf16 H (from the sigmoid GELU' needs
+ * anyway) into the workspace, and dB = G^T dY reads it there. dX, dA, da and db are bitwise
+ * those of mlp_tp_backward; dB differs only by G being recomputed from the rounded H.
+ * Workspace (256-byte aligned, at least mlp_tp_recompute_workspace_bytes): dH [T,f] bf16 |
+ * G [T,f] bf16 | the reduction partials; dH and G are there on return. Other arguments and
+ * errors as mlp_tp_backward. */
+size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t);
+mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
+                                     const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX, mlp_bf16* dA,
+                                     mlp_bf16* dB, float* da, float* db, void* workspace, size_t workspace_bytes,
+                                     void* cuda_stream);
+
 /* Synchronises `cuda_stream`, then reports and clears the device status word of the
  * current device: MLP_ETIMEOUT if a bounded device wait ran out since the last query,
  * MLP_ECUDA if the stream holds a CUDA error, else MLP_OK. */

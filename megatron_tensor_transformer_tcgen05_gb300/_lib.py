@@ -90,6 +90,10 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_attn_workspace_bytes.argtypes = [i32] * 6
             L.mlp_tp_attn_backward.restype = i32
             L.mlp_tp_attn_backward.argtypes = [vp] * 7 + [i32] * 7 + [vp] * 4 + [sz, vp]
+            L.mlp_tp_recompute_workspace_bytes.restype = sz
+            L.mlp_tp_recompute_workspace_bytes.argtypes = [i32] * 4
+            L.mlp_tp_backward_recompute.restype = i32
+            L.mlp_tp_backward_recompute.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 5 + [vp, sz, vp]
             _lib = L
     return _lib
 
@@ -230,3 +234,14 @@ def mlp_tp_attn_backward(X, Wqkv, Wo, QKV, C, L, dY, b: int, s: int, h: int, a: 
     _check(lib().mlp_tp_attn_backward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(QKV), _ptr(C), _ptr(L), _ptr(dY), b, s, h,
                                       a, d, t, int(bool(causal)), _ptr(dX), _ptr(dWqkv), _ptr(dWo), _ptr(workspace),
                                       workspace_bytes, _stream(stream)), "mlp_tp_attn_backward")
+
+
+def mlp_tp_recompute_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
+    return int(lib().mlp_tp_recompute_workspace_bytes(T, h, f, t))
+
+
+def mlp_tp_backward_recompute(X, A, B, H, dY, T: int, h: int, f: int, t: int, dX, dA, dB, da, db, workspace,
+                              workspace_bytes: int, stream=None) -> None:
+    _check(lib().mlp_tp_backward_recompute(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(dY), T, h, f, t, _ptr(dX),
+                                           _ptr(dA), _ptr(dB), _ptr(da), _ptr(db), _ptr(workspace), workspace_bytes,
+                                           _stream(stream)), "mlp_tp_backward_recompute")

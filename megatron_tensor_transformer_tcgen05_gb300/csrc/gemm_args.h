@@ -16,6 +16,7 @@ enum Epi : int {
     EPI_BIAS_DROPOUT_RES = 4,
     EPI_SWIGLU = 5,   // dual B operand: D = [X A | X Wg] per 128 output columns -> Ha, Hg, U
     EPI_DSWIGLU = 6,  // dU = acc; dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha) -> dHa, dHg
+    EPI_DGELU_G = 7,  // as EPI_DGELU, and G = GELU(H) recomputed from the same sigmoid -> dH, G
 };
 
 struct GemmArgs {
@@ -30,7 +31,7 @@ struct GemmArgs {
     int n_fastest;               // tile order: 0 = M index fastest, 1 = N index fastest
     int raster_group;            // tiles of the fast index per group (<= 0: all of them)
     const __nv_bfloat16* bias;   // [N] for EPI_BIAS / EPI_BIAS_GELU
-    const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU; residual R for EPI_BIAS_DROPOUT_RES
+    const __nv_bfloat16* aux;    // H [M, ld_aux] for EPI_DGELU(_G); residual R for EPI_BIAS_DROPOUT_RES
     float* colsum_rows;          // EPI_DGELU, optional: per-32-row column sums of D (fp32),
                                  // [ceil(M/32), N] row-major; NULL = not wanted
     const __nv_bfloat16* aux2;   // Hg [M, ld_aux] for EPI_DSWIGLU (aux is Ha)

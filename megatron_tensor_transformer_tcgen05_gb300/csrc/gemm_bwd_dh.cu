@@ -1,8 +1,12 @@
-// Backward GEMM 3: dH = (dY*B^T) (.) GELU'(H) (both operands K-major).
+// Backward GEMM 3: dH = (dY*B^T) (.) GELU'(H) (both operands K-major); the _G flavour also
+// writes G = GELU(H) for a backward that recomputes G.
 #include "umma_gemm.cuh"
 
 namespace mlp {
 template cudaError_t launch_umma_gemm<128, false, false, EPI_DGELU, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU, 2>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<128, false, false, EPI_DGELU_G, 1>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU_G, 1>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU_G, 2>(const GemmArgs&, int, cudaStream_t);
 }  // namespace mlp

@@ -395,22 +395,29 @@ mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, u
     return MLP_OK;
 }
 
-mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
-                           const mlp_bf16* G, const mlp_bf16* dY, int T, int h, int f, int t,
-                           mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
-                           void* workspace, size_t workspace_bytes, void* cuda_stream)
+}  // extern "C"
+
+namespace mlp {
+
+// The backward pass. With G == NULL the dH GEMM also recomputes G = GELU(H) into the
+// workspace (after dH) and GEMM 6 reads it from there.
+static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
+                                const mlp_bf16* G, const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX,
+                                mlp_bf16* dA, mlp_bf16* dB, float* da, float* db, void* workspace,
+                                size_t workspace_bytes, void* cuda_stream)
 {
+    const bool recompute = (G == nullptr);
     mlp_status st = check_shape(T, h, f, t);
     if (st != MLP_OK) return st;
     // Token-indexed buffers may be NULL only when there are no tokens.
-    if (!A || !B || !dA || !dB || !da || !db || !workspace ||
-        (T > 0 && (!X || !H || !G || !dY || !dX)))
+    if (!A || !B || !dA || !dB || !da || !db || !workspace || (T > 0 && (!X || !H || !dY || !dX)))
         return MLP_EINVAL;
     const void* ptrs[] = {X, A, B, H, G, dY, dX, dA, dB, da, db};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
-    if (workspace_bytes < mlp_tp_workspace_bytes(T, h, f, t)) return MLP_EWORKSPACE;
+    const size_t need = recompute ? mlp_tp_recompute_workspace_bytes(T, h, f, t) : mlp_tp_workspace_bytes(T, h, f, t);
+    if (workspace_bytes < need) return MLP_EWORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != MLP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -427,24 +434,31 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
-    float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f));
-    float* dy_part = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + ws_rows_bytes(T, f));
+    const size_t g_bytes = recompute ? ws_dh_bytes(T, f) : 0;  // the recomputed G follows dH
+    mlp_bf16* Gw = recompute ? reinterpret_cast<mlp_bf16*>(ws + ws_dh_bytes(T, f)) : nullptr;
+    float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + g_bytes);
+    float* dy_part = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + g_bytes + ws_rows_bytes(T, f));
+    const mlp_bf16* Gin = recompute ? Gw : G;
     const int nsplit = colsum_splits(T);
     CallTimer timer(s);
 
-    // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h.
+    // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h. When
+    // recomputing, the same epilogue also writes G = GELU(H).
     GemmArgs g3{};
     if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, kmajor_b_box(T, bn_f)) ||
         !map_store(&g3.tmD0, dH, f, T))
         return MLP_ECUDA;
     g3.tmD1 = g3.tmD0;
+    if (recompute && !map_store(&g3.tmD1, Gw, f, T)) return MLP_ECUDA;
     g3.M = T; g3.N = f; g3.K = h;
     g3.aux = reinterpret_cast<const __nv_bfloat16*>(H);
     g3.ld_aux = f;
     g3.colsum_rows = dh_rows;  // da's per-32-row partial sums come out of this epilogue
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
-    if (gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const cudaError_t e3 = recompute ? gemm<false, false, EPI_DGELU_G>(g3, bn_f, dev->num_sms, s)
+                                     : gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s);
+    if (e3 != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DH);
 
     // GEMM 4: dX = sum over shards of dH_i*A_i^T; A [h,f] is K-major for N = h, K = f.
@@ -473,7 +487,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
 
     // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major.
     GemmArgs g6{};
-    if (!map_mnmajor(&g6.tmA, G, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) ||
+    if (!map_mnmajor(&g6.tmA, Gin, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) ||
         !map_store(&g6.tmD0, dB, h, f))
         return MLP_ECUDA;
     g6.tmD1 = g6.tmD0;
@@ -495,6 +509,34 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_COLSUM_FINAL);
     return MLP_OK;
+}
+
+}  // namespace mlp
+
+extern "C" {
+
+mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
+                           const mlp_bf16* G, const mlp_bf16* dY, int T, int h, int f, int t,
+                           mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    if (T > 0 && !G) return MLP_EINVAL;
+    return backward_impl(X, A, B, H, G, dY, T, h, f, t, dX, dA, dB, da, db, workspace, workspace_bytes, cuda_stream);
+}
+
+size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t)
+{
+    if (check_shape(T, h, f, t) != MLP_OK) return 0;
+    return 2 * ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
+}
+
+mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
+                                     const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX, mlp_bf16* dA,
+                                     mlp_bf16* dB, float* da, float* db, void* workspace, size_t workspace_bytes,
+                                     void* cuda_stream)
+{
+    return backward_impl(X, A, B, H, nullptr, dY, T, h, f, t, dX, dA, dB, da, db, workspace, workspace_bytes,
+                         cuda_stream);
 }
 
 mlp_status mlp_tp_query_device_status(void* cuda_stream)

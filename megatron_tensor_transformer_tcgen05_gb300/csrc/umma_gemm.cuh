@@ -22,6 +22,8 @@
 //                  (keep from Philox4x32-10 on the element's index; philox.cuh)
 //   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH (and, optionally,
 //                  its column sums over each 32-row block in fp32, for the bias gradient)
+//   EPI_DGELU_G    as EPI_DGELU, and G = GELU(H[m,n]) from the same sigmoid -> stores dH, G
+//                  (the backward that recomputes G instead of keeping it from the forward)
 //   EPI_PLAIN      D = acc                                 -> stores D
 //   EPI_SWIGLU     acc = [X A | X Wg] over 128 columns: Ha, Hg, U = SiLU(Ha) Hg -> stores all three
 //   EPI_DSWIGLU    dU = acc: dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha)            -> stores both
@@ -55,7 +57,8 @@ struct GemmCfg {
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int NOUT = (EPI == EPI_SWIGLU) ? 3 : (EPI == EPI_BIAS_GELU || EPI == EPI_DSWIGLU) ? 2 : 1;
+    static constexpr int NOUT =
+        (EPI == EPI_SWIGLU) ? 3 : (EPI == EPI_BIAS_GELU || EPI == EPI_DSWIGLU || EPI == EPI_DGELU_G) ? 2 : 1;
     static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
     static constexpr uint32_t EPI_BYTES = 4 * 2 * NOUT * STG_BYTES;  // 4 warps x 2 buffers
     static constexpr uint32_t TMEM_COLS = 2 * BN;                    // two fp32 accumulators
@@ -94,6 +97,20 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float x)
     const float u = k0 * x * fmaf(k1, x2, 1.0f);
     const float e = __expf(-2.0f * u);
     const float s = __fdividef(1.0f, 1.0f + e);
+    const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
+    return fmaf(2.0f * x * s * (1.0f - s), du, s);
+}
+
+// GELU'(x) as gelu_tanh_grad_f (same operations, so the same bits), and GELU(x) in g from
+// the same sigmoid, as gelu_tanh_f computes it.
+__device__ __forceinline__ float gelu_tanh_grad_and_value_f(float x, float& g)
+{
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float x2 = x * x;
+    const float u = k0 * x * fmaf(k1, x2, 1.0f);
+    const float e = __expf(-2.0f * u);
+    const float s = __fdividef(1.0f, 1.0f + e);
+    g = x * s;
     const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
     return fmaf(2.0f * x * s * (1.0f - s), du, s);
 }
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
             uint4 hnext[4], gnext[4];
-            if (EPI == EPI_DGELU || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
+            if (EPI == EPI_DGELU || EPI == EPI_DGELU_G || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int n = n0 + 8 * i;
@@ -549,7 +566,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                             v[4 * g + w] = rv[4 * g + w] + (((kb >> w) & 1u) ? v[4 * g + w] * args.drop.scale : 0.0f);
                     }
                 }
-                if (EPI == EPI_DGELU) {
+                if (EPI == EPI_DGELU || EPI == EPI_DGELU_G) {
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
@@ -562,8 +579,16 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                                            : make_uint4(0, 0, 0, 0);
                         }
                     }
+                    if (EPI == EPI_DGELU_G) {
+                        float gv[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(hv[j]);
+                        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_and_value_f(hv[j], gv[j]);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) p1[j] = pack_bf16x2(gv[2 * j], gv[2 * j + 1]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(hv[j]);
+                    }
                     if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
                         float cs[32];
 #pragma unroll
