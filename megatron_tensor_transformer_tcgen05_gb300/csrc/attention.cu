@@ -9,12 +9,12 @@
 // mask implicit, section 4 "kernel fusion"). Here the whole of S -> P -> C also stays on
 // chip: S is never written to HBM.
 //
-// Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 320 threads.
-//   warp 0     TMA: the Q block once, then K and V blocks of 128 keys through a 4-slot ring
+// Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 192 threads, two
+// CTAs per SM (one's softmax overlaps the other's MMAs).
+//   warp 0     TMA: the Q block once, then K and V blocks of 64 keys through two 2-slot rings
 //   warp 1     TMEM allocation and every tcgen05.mma: S_j = Q K_j^T into one of two TMEM
 //              S buffers, O += P_j V_j into the TMEM output accumulator
-//   warps 2-9  softmax, two threads per query row r (TMEM lane r), each on half of the
-//              block's columns: read S_j from TMEM, mask,
+//   warps 2-5  softmax, thread r <-> query row r (TMEM lane r): read S_j from TMEM, mask,
 //              running row max and sum (base 2), P_j -> shared memory (bf16, the A operand
 //              of the next MMA); rescale O in TMEM only when the row max has grown by more
 //              than 2^8 since the last rescale (the final division by the row sum makes the
@@ -194,37 +194,44 @@ __device__ __forceinline__ float sum_tree(const float (&x)[N])
 }
 
 struct FwdCfg {
-    static constexpr int BQ = 128, BKV = 128;
-    static constexpr int THREADS = 320;  // producer, MMA, 8 softmax warps (two threads per row)
-    static constexpr uint32_t TILE = 128 * kHeadDim * 2;  // a 128 x 128 bf16 tile: 32 KB
-    // K and V blocks share one ring of slots, loaded K_0 V_0 K_1 V_1 ...; a K slot is freed as
-    // soon as its S MMA completes and a V slot when its PV MMA completes, so the loads run
-    // ahead of the softmax instead of waiting for the PV product.
-    static constexpr int SLOTS = 4;
-    static constexpr uint32_t OFF_Q = 0, OFF_KV = TILE, OFF_P = (1 + SLOTS) * TILE, OFF_X = (2 + SLOTS) * TILE,
-                              OFF_BAR = OFF_X + 2 * 2 * 128 * 4;
-    // barriers: q | full[4] | empty[4] | sfull[2] | sfree[2] | pfull | pvdone | drain | pair[4][2]
-    static constexpr int NUM_BARS = 1 + 2 * SLOTS + 4 + 3 + 8;
-    static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+    static constexpr int BQ = 128, BKV = 64;
+    // producer, MMA, 4 softmax warps (one thread per query row); two CTAs share an SM, so one
+    // CTA's softmax runs while the other's MMAs keep the tensor pipe busy
+    static constexpr int THREADS = 192;
+    static constexpr uint32_t QTILE = 128 * kHeadDim * 2;  // Q block: 32 KB
+    static constexpr uint32_t KVTILE = 64 * kHeadDim * 2;  // K or V block: 16 KB
+    static constexpr uint32_t PTILE = 128 * 64 * 2;        // P block: 16 KB
+    // K and V blocks have a ring of two slots each (slots 0-1 hold K, 2-3 hold V). A K slot is
+    // freed as soon as its S MMA completes and a V slot when its PV MMA completes; the
+    // producer issues K_0 K_1 and then V_j, K_{j+2} for each j, so a K load never queues
+    // behind a V load that waits for a later PV.
+    static constexpr uint32_t OFF_Q = 0, OFF_KV = QTILE, OFF_P = QTILE + 4 * KVTILE, OFF_BAR = OFF_P + PTILE;
+    // barriers: q | full[4] | empty[4] | sfull[2] | sfree[2] | pfull | pvdone | drain
+    static constexpr int NUM_BARS = 1 + 8 + 4 + 3;
+    // No alignment slack (two CTAs must fit in one SM's shared memory): the kernel checks
+    // that its dynamic shared memory starts on a 1 KB boundary and otherwise does nothing.
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);
-    static constexpr uint32_t TMEM_COLS = 512;  // S[0] 0..127 | S[1] 128..255 | O 256..383
-    static constexpr uint32_t O_COL = 256;
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static constexpr uint32_t TMEM_COLS = 256;  // S[0] 0..63 | S[1] 64..127 | O 128..255
+    static constexpr uint32_t O_COL = 128;
+    static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
-__global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = FwdCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV, sP = base + C::OFF_P, sX = base + C::OFF_X;
+    const uint32_t base = smem_u32(smem_raw);
+    if ((base & 1023u) != 0) {  // uniform: every thread leaves before any barrier or TMEM use
+        if (threadIdx.x == 0) atomicCAS(args.status, 0, DEV_SMEM_MISALIGNED);
+        return;
+    }
+    uint8_t* gbase = smem_raw;
+    const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV, sP = base + C::OFF_P;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 8 * C::SLOTS, b_sf = b_empty + 8 * C::SLOTS,
-                   b_sfree = b_sf + 16, b_pf = b_sfree + 16, b_pv = b_pf + 8, b_drain = b_pv + 8,
-                   b_pair = b_drain + 8;
+    const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 32, b_sf = b_empty + 32, b_sfree = b_sf + 16,
+                   b_pf = b_sfree + 16, b_pv = b_pf + 8, b_drain = b_pv + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     const int qb = nqb - 1 - static_cast<int>(blockIdx.x) % nqb;
     const int q0 = qb * C::BQ;
     const int nkb_all = (s + C::BKV - 1) / C::BKV;
-    const int nkb = args.causal ? min(nkb_all, qb + 1) : nkb_all;
+    const int nkb = args.causal ? min(nkb_all, (q0 + C::BQ - 1) / C::BKV + 1) : nkb_all;
     const int row0 = bi * s;
     const int hd = a * kHeadDim;
     const int colQ = head * kHeadDim, colK = hd + colQ, colV = 2 * hd + colQ;
@@ -245,18 +252,17 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
-        for (int i = 0; i < C::SLOTS; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(b_full + 8 * i, 1);
             mbar_init(b_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sf + 8 * i, 1);
-            mbar_init(b_sfree + 8 * i, 8);
+            mbar_init(b_sfree + 8 * i, 4);
         }
-        mbar_init(b_pf, 8);
+        mbar_init(b_pf, 4);
         mbar_init(b_pv, 1);
         mbar_init(b_drain, 1);
-        for (int i = 0; i < 8; ++i) mbar_init(b_pair + 8 * i, 2);  // the two warps of a row quadrant
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&args.tmQ);
@@ -277,99 +283,93 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
             // drain indices: 0 = q, 1 + i = full[i]
             uint32_t issued = 1u, par = 0u;
             bool ok = true;
-            mbar_arrive_expect_tx(b_q, C::TILE);
+            mbar_arrive_expect_tx(b_q, C::QTILE);
             tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_q);
-            tma_load_2d(sQ + C::TILE / 2, &args.tmQ, colQ + 64, row0 + q0, b_q);
-            for (int n = 0; n < 2 * nkb; ++n) {  // n = 2j: K_j, n = 2j + 1: V_j
-                const int slot = n % C::SLOTS;
-                const uint32_t ph = static_cast<uint32_t>(n / C::SLOTS) & 1u;
-                if (n >= C::SLOTS && !mbar_wait_bounded(b_empty + 8 * slot, ph ^ 1u, abort_flag, args.status, limit,
-                                                        DEV_TIMEOUT_PRODUCER, 1000, n)) {
+            tma_load_2d(sQ + C::QTILE / 2, &args.tmQ, colQ + 64, row0 + q0, b_q);
+            // load order K_0 K_1 V_0 K_2 V_1 K_3 ...: step n < 2 is K_n; then V_j, K_{j+2}
+            for (int n = 0; n < 2 * nkb + 2; ++n) {
+                const bool isv = n >= 2 && (n & 1) == 0;
+                const int j = n < 2 ? n : (isv ? (n - 2) >> 1 : ((n - 3) >> 1) + 2);
+                if (j >= nkb) continue;  // K_{j+2} past the last block
+                const int slot = (isv ? 2 : 0) + (j & 1);
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (j >= 2 && !mbar_wait_bounded(b_empty + 8 * slot, ph ^ 1u, abort_flag, args.status, limit,
+                                                 DEV_TIMEOUT_PRODUCER, 1000, n)) {
                     ok = false;
                     break;
                 }
-                const int y = row0 + (n >> 1) * C::BKV;
-                const int x = (n & 1) ? colV : colK;
-                const uint32_t dst = sKV + slot * C::TILE, fb = b_full + 8 * slot;
-                mbar_arrive_expect_tx(fb, C::TILE);
+                const int y = row0 + j * C::BKV;
+                const int x = isv ? colV : colK;
+                const uint32_t dst = sKV + slot * C::KVTILE, fb = b_full + 8 * slot;
+                mbar_arrive_expect_tx(fb, C::KVTILE);
                 tma_load_2d(dst, &args.tmKV, x, y, fb);
-                tma_load_2d(dst + C::TILE / 2, &args.tmKV, x + 64, y, fb);
+                tma_load_2d(dst + C::KVTILE / 2, &args.tmKV, x + 64, y, fb);
                 issued |= 1u << (1 + slot);
                 par = (par & ~(1u << (1 + slot))) | (ph << (1 + slot));
             }
-            if (!ok) drain_loads(bar, 1 + C::SLOTS, issued, par, args.status);
+            if (!ok) drain_loads(bar, 5, issued, par, args.status);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_q, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 1001, -1);
             bool any = false;
-            const uint64_t dQ = desc_k(sQ), dKV = desc_k(sKV), dP = desc_k(sP), dV = desc_mn(sKV, C::TILE / 2);
-            for (int j = 0; ok && j <= nkb; ++j) {
-                if (j < nkb) {  // S_j = Q K_j^T
-                    const int st = j & 1, n = 2 * j, slot = n % C::SLOTS;
-                    if (!mbar_wait_bounded(b_full + 8 * slot, (n / C::SLOTS) & 1, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_FULL, 1002, j) ||
-                        (j >= 2 && !mbar_wait_bounded(b_sfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
-                                                      limit, DEV_TIMEOUT_MMA_ACC, 1003, j))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t dK = desc_at(dKV, slot * C::TILE);
+            const uint64_t dQ = desc_k(sQ), dKV = desc_k(sKV), dP = desc_k(sP), dV = desc_mn(sKV, C::KVTILE / 2);
+            // S_j = Q K_j^T into TMEM score buffer j % 2
+            auto issue_s = [&](int j) -> bool {
+                const int st = j & 1;
+                if (!mbar_wait_bounded(b_full + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
+                                       DEV_TIMEOUT_MMA_FULL, 1002, j) ||
+                    (j >= 2 && !mbar_wait_bounded(b_sfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                                  DEV_TIMEOUT_MMA_ACC, 1003, j)))
+                    return false;
+                tc_fence_after();
+                const uint64_t dK = desc_at(dKV, st * C::KVTILE);
 #pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint32_t off = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + 128u * st, desc_at(dQ, off), desc_at(dK, off), C::IDESC_S, k > 0);
-                    }
-                    any = true;
-                    umma_commit(b_sf + 8 * st);
-                    umma_commit(b_empty + 8 * slot);
+                for (int k = 0; k < kHeadDim / 16; ++k) {
+                    const uint32_t oq = (C::QTILE / 2) * (k >> 2) + 32u * (k & 3);
+                    const uint32_t ok2 = (C::KVTILE / 2) * (k >> 2) + 32u * (k & 3);
+                    umma_bf16(tmem + 64u * st, desc_at(dQ, oq), desc_at(dK, ok2), C::IDESC_S, k > 0);
                 }
-                if (j >= 1) {  // O += P_{j-1} V_{j-1}
-                    const int pj = j - 1, n = 2 * pj + 1, slot = n % C::SLOTS;
-                    if (!mbar_wait_bounded(b_pf, pj & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 1004,
-                                           pj) ||
-                        !mbar_wait_bounded(b_full + 8 * slot, (n / C::SLOTS) & 1, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_FULL, 1005, pj)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t dVs = desc_at(dV, slot * C::TILE);
+                any = true;
+                umma_commit(b_sf + 8 * st);
+                umma_commit(b_empty + 8 * st);
+                return true;
+            };
+            // Scores run two blocks ahead: S_0, S_1, then after each P_j: PV_j and S_{j+2}.
+            for (int j = 0; ok && j < 2 && j < nkb; ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < nkb; ++j) {  // O += P_j V_j
+                const int vs = 2 + (j & 1);
+                if (!mbar_wait_bounded(b_pf, j & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 1004, j) ||
+                    !mbar_wait_bounded(b_full + 8 * vs, (j >> 1) & 1, abort_flag, args.status, limit,
+                                       DEV_TIMEOUT_MMA_FULL, 1005, j)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dVs = desc_at(dV, vs * C::KVTILE);
 #pragma unroll
-                    for (int k = 0; k < C::BKV / 16; ++k) {
-                        const uint32_t aoff = (C::TILE / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + C::O_COL, desc_at(dP, aoff), desc_at(dVs, 2048u * k), C::IDESC_PV,
-                                  (pj > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(b_pv);
-                    umma_commit(b_empty + 8 * slot);
-                }
+                for (int k = 0; k < C::BKV / 16; ++k)
+                    umma_bf16(tmem + C::O_COL, desc_at(dP, 32u * k), desc_at(dVs, 2048u * k), C::IDESC_PV,
+                              (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(b_pv);
+                umma_commit(b_empty + 8 * vs);
+                if (j + 2 < nkb) ok = issue_s(j + 2);
             }
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
         // ------------------------------ softmax -----------------------------------
-        // Two threads per query row: warp w (2..9) reads TMEM lanes of quadrant w % 4 and
-        // columns [64 half, 64 half + 64) of each block, half = (w - 2) / 4. The pair shares
-        // its row max through shared memory (double-buffered; an mbarrier per quadrant and
-        // buffer, waited with the usual bound), so both apply the same reference and rescale
-        // decisions.
-        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are the ones this warp may read
         const int r = 32 * q + lane;
         const int qi = q0 + r;
-        const int cb = 64 * half;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        const uint32_t x_mine = sX + static_cast<uint32_t>((half * 128 + r) * 4);
-        const uint32_t x_peer = sX + static_cast<uint32_t>(((1 - half) * 128 + r) * 4);
         const float NEG_INF = -__int_as_float(0x7f800000);
         const float c2 = args.scale_log2;
         float m_used = NEG_INF, l = 0.0f;  // m_used in base-2 units of the scaled scores
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
             const int st = j & 1;
-            const uint32_t xb = static_cast<uint32_t>(j & 1) * (2 * 128 * 4);
             if (!warp_wait(b_sf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1006, j)) {
                 ok = false;
                 break;
@@ -378,8 +378,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
             float x[64];
             {
                 uint32_t u0[32], u1[32];
-                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
-                tmem_ld_32x32b_x32(t_lane + 128u * st + cb + 32u, u1);
+                tmem_ld_32x32b_x32(t_lane + 64u * st, u0);
+                tmem_ld_32x32b_x32(t_lane + 64u * st + 32u, u1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -390,23 +390,15 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_sfree + 8 * st);
-            const int k0 = j * C::BKV + cb;
-            if ((args.causal && j * C::BKV + C::BKV - 1 > q0) || j * C::BKV + C::BKV > s) {  // CTA-uniform
+            const int k0 = j * C::BKV;
+            if ((args.causal && k0 + C::BKV - 1 > q0) || k0 + C::BKV > s) {  // CTA-uniform
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int key = k0 + c;
                     if (key >= s || (args.causal && key > qi)) x[c] = NEG_INF;
                 }
             }
-            sts_f32(x_mine + xb, max_tree(x));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_pair + 8 * (2 * q + (j & 1)));
-            if (!warp_wait(b_pair + 8 * (2 * q + (j & 1)), (j >> 1) & 1, abort_flag, args.status, limit,
-                           DEV_TIMEOUT_EPILOGUE, 1010, j)) {
-                ok = false;
-                break;
-            }
-            const float mx = fmaxf(lds_f32(x_mine + xb), lds_f32(x_peer + xb)) * c2;  // scale > 0: commutes
+            const float mx = max_tree(x) * c2;  // the scale is positive: max commutes with it
             const bool resc = mx > m_used + static_cast<float>(kLazyRescaleLog2);
             float alpha = 1.0f;
             if (resc) {
@@ -424,12 +416,12 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
                     ok = false;
                     break;
                 }
-                if (__any_sync(0xffffffffu, resc)) {  // rescale this half of the O row in place
+                if (__any_sync(0xffffffffu, resc)) {  // rescale the O row in place
                     tc_fence_after();
                     uint32_t o[32];
 #pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        const uint32_t ta = t_lane + C::O_COL + cb + 32u * c;
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        const uint32_t ta = t_lane + C::O_COL + 32u * c;
                         tmem_ld_32x32b_x32(ta, o);
                         tmem_ld_wait();
 #pragma unroll
@@ -439,7 +431,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
                     tmem_st_wait();
                 }
             }
-            store_row_part_sw128<64, C::BQ>(sP, r, cb, x);
+            store_row_sw128<64, C::BQ>(sP, r, x);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -448,23 +440,16 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         if (ok && nkb > 0 &&
             warp_wait(b_pv, (nkb - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
             tc_fence_after();
-            const uint32_t xb = static_cast<uint32_t>(nkb & 1) * (2 * 128 * 4);
-            sts_f32(x_mine + xb, l);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_pair + 8 * (2 * q + (nkb & 1)));
-            const bool paired = warp_wait(b_pair + 8 * (2 * q + (nkb & 1)), (nkb >> 1) & 1, abort_flag, args.status,
-                                          limit, DEV_TIMEOUT_EPILOGUE, 1011, nkb);
-            const float lt = l + lds_f32(x_peer + xb);  // both halves used the same references
-            const float inv_l = lt > 0.0f ? 1.0f / lt : 0.0f;
-            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ + cb;
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ;
             uint32_t o[32];
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::O_COL + cb + 32u * c, o);
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                tmem_ld_32x32b_x32(t_lane + C::O_COL + 32u * c, o);
                 tmem_ld_wait();
-                if (paired && qi < s) store32_global(dst + 32 * c, o, inv_l);
+                if (qi < s) store32_global(dst + 32 * c, o, inv_l);
             }
-            if (paired && half == 0 && qi < s) args.lse[static_cast<size_t>(bh) * s + qi] = m_used + log2f(lt);
+            if (qi < s) args.lse[static_cast<size_t>(bh) * s + qi] = m_used + log2f(l);
         }
     }
 
@@ -1006,6 +991,10 @@ cudaError_t launch_tile_kernel(K kern, const AttnArgs& args, int blocks_y, cudaS
 {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    // all of the SM's unified L1 / shared memory as shared memory (the forward kernel needs it
+    // for two CTAs per SM)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     const long long grid = static_cast<long long>(args.b) * args.a * blocks_y;
     if (grid <= 0) return cudaSuccess;

@@ -912,8 +912,9 @@ extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqk
 
     // Per head: scores, mask, softmax and P V on chip; C and L to HBM.
     AttnArgs at = attn_args(dev, b, s, a, causal);
-    if (!make_map(&at.tmQ, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return MLP_ECUDA;
-    at.tmKV = at.tmQ;
+    if (!make_map(&at.tmQ, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&at.tmKV, QKV, 3 * hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLP_ECUDA;
     at.out = reinterpret_cast<__nv_bfloat16*>(Cctx);
     at.lse = L;
     if (launch_attn_fwd(at, strm) != cudaSuccess) return MLP_ECUDA;

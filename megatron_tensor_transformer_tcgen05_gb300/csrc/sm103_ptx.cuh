@@ -17,6 +17,8 @@ enum : int {
     DEV_TIMEOUT_EPILOGUE = 4,   // epilogue gave up waiting for a finished accumulator
     DEV_TIMEOUT_DRAIN = 5,      // in-flight copies did not land within the drain limit
     DEV_TIMEOUT_SELFTEST = 6,   // the self-test wait ran out, as it is meant to
+    DEV_SMEM_MISALIGNED = 7,    // dynamic shared memory did not start on the 1 KB boundary a kernel
+                                // without alignment slack needs; the kernel did nothing
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
