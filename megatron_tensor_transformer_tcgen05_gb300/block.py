@@ -66,15 +66,26 @@ def empty_swiglu_buffers(T: int, h: int, f: int, t: int, device="cuda") -> dict[
     return out
 
 
-def swiglu_step(inp: dict, buf: dict, t: int, stream=None) -> None:
-    """One forward + backward of the SwiGLU block."""
-    from ._lib import mlp_tp_swiglu_backward, mlp_tp_swiglu_forward
+def swiglu_forward(inp: dict, buf: dict, t: int, stream=None) -> None:
+    from ._lib import mlp_tp_swiglu_forward
     T, h = inp["X"].shape
     f = inp["A"].shape[1]
     mlp_tp_swiglu_forward(inp["X"], inp["A"], inp["Wg"], inp["B"], T, h, f, t, buf["Ha"], buf["Hg"], buf["U"],
                           buf["Y"], stream)
+
+
+def swiglu_backward(inp: dict, buf: dict, t: int, stream=None) -> None:
+    from ._lib import mlp_tp_swiglu_backward
+    T, h = inp["X"].shape
+    f = inp["A"].shape[1]
     mlp_tp_swiglu_backward(inp["X"], inp["A"], inp["Wg"], inp["B"], buf["Ha"], buf["Hg"], buf["U"], inp["dY"], T, h,
                            f, t, buf["dX"], buf["dA"], buf["dWg"], buf["dB"], buf["ws"], buf["ws"].numel(), stream)
+
+
+def swiglu_step(inp: dict, buf: dict, t: int, stream=None) -> None:
+    """One forward + backward of the SwiGLU block."""
+    swiglu_forward(inp, buf, t, stream)
+    swiglu_backward(inp, buf, t, stream)
 
 
 # ---- head-parallel attention block ----------------------------------------------------------
