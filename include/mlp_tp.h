@@ -186,7 +186,8 @@ int mlp_tp_last_device_where(int* block, int* thread, int* tile, int* kblock);
 /* Human-readable name of a status. Never NULL. */
 const char* mlp_tp_status_string(mlp_status s);
 
-/* Number of kernel launches one forward / one backward call makes for these sizes. */
+/* Number of kernel launches one mlp_tp_forward / mlp_tp_backward call makes for these sizes
+ * (the attention block's calls make 3 and 7). */
 int mlp_tp_launches_per_call(int backward, int T);
 
 /* Self-test of the bounded-wait path: launches one small kernel that waits on a barrier

@@ -5,9 +5,9 @@
 //   S = Q K^T / sqrt(d),  key j > query i masked when causal,  P = softmax_rows(S),  C = P V
 // ("Efficient Large-Scale Language Model Training on GPU Clusters Using Megatron-LM",
 // section 3, Figure 5b: each tensor-parallel shard runs whole heads, so the softmax never
-// crosses a shard; the pages fuse scale, mask and softmax into one kernel with the causal
-// mask implicit, section 4 "kernel fusion"). Here the whole of S -> P -> C also stays on
-// chip: S is never written to HBM.
+// crosses a shard; and its "Computation Optimizations: Fused Kernels and Data Layout" fuses
+// scale, mask and softmax into one kernel with the causal mask implicit). Here the whole of
+// S -> P -> C also stays on chip: S is never written to HBM.
 //
 // Forward (attn_fwd_kernel): one CTA per (sequence, head, 128-query block), 192 threads, two
 // CTAs per SM (one's softmax overlaps the other's MMAs).
@@ -105,13 +105,6 @@ __device__ __forceinline__ void store_row_part_sw128(uint32_t buf, int r, int c0
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ float lds_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 // 32 fp32 values * mul -> 32 bf16 at dst (64 bytes, 16-byte aligned).

@@ -1,5 +1,6 @@
-// mlp_tp_api.cu -- the C ABI of include/mlp_tp.h: argument checks, TMA tensor maps,
-// launch sequencing of the forward (2 kernels) and backward (6 kernels) passes, and the
+// mlp_tp_api.cu -- the C ABI of include/mlp_tp.h: argument checks, TMA tensor maps, launch
+// sequencing of the MLP block's forward (2 kernels) and backward (6 kernels), of its dropout,
+// SwiGLU and GELU-recompute variants and of the attention block (3 + 7 kernels), and the
 // device status word that bounded waits report into.
 #include <cuda.h>
 #include <cuda_runtime.h>
