@@ -55,7 +55,9 @@ typedef enum {
                              f/t not multiples of 8; attention: a % t != 0, d != 128) */
     MLP_EALIGN = 3,       /* a pointer is not 16-byte aligned */
     MLP_ECUDA = 4,        /* a CUDA runtime call or launch failed */
-    MLP_ETIMEOUT = 5,     /* a bounded device-side wait ran out (reported by query) */
+    MLP_ETIMEOUT = 5,     /* a device-side check failed, reported by query: a bounded wait ran
+                             out, or (device code 7) a kernel found its dynamic shared memory
+                             off its 1 KB alignment and did nothing */
     MLP_EUNSUPPORTED = 6, /* no sm_100-family tensor cores on the current device */
     MLP_EWORKSPACE = 7    /* workspace smaller than mlp_tp_workspace_bytes() */
 } mlp_status;

@@ -250,7 +250,7 @@ const char* mlp_tp_status_string(mlp_status s)
     case MLP_ESHAPE: return "MLP_ESHAPE: a size breaks the call's shape rules (f % t, multiples of 8, a % t, d)";
     case MLP_EALIGN: return "MLP_EALIGN: pointer not 16-byte aligned";
     case MLP_ECUDA: return "MLP_ECUDA: CUDA runtime error";
-    case MLP_ETIMEOUT: return "MLP_ETIMEOUT: a bounded device wait ran out";
+    case MLP_ETIMEOUT: return "MLP_ETIMEOUT: a device-side check failed (a bounded wait ran out, or see mlp_tp_last_device_code)";
     case MLP_EUNSUPPORTED: return "MLP_EUNSUPPORTED: current device is not sm_103";
     case MLP_EWORKSPACE: return "MLP_EWORKSPACE: workspace too small";
     }

@@ -79,3 +79,50 @@ def test_binding_raises_named_error(L):
     with pytest.raises(_lib.MlpError) as ei:
         _lib.mlp_tp_forward(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 64, 256, 3, FAKE, FAKE, FAKE, stream=0)
     assert ei.value.name == "MLP_ESHAPE"
+
+
+def test_attention_workspace_and_shape_rules():
+    b, s, h, a, d = 2, 200, 256, 2, 128
+    ws = _lib.mlp_tp_attn_workspace_bytes(b, s, h, a, d, 2)
+    T, hd = b * s, a * d
+    assert ws >= T * hd * 2 + b * a * s * 4 + T * 3 * hd * 2  # dC | D | dQKV
+    assert _lib.mlp_tp_attn_workspace_bytes(b, s, h, a, 64, 1) == 0    # d != 128
+    assert _lib.mlp_tp_attn_workspace_bytes(b, s, h, 3, d, 2) == 0     # a % t
+    assert _lib.mlp_tp_attn_workspace_bytes(b, s, 250, a, d, 1) == 0   # h % 8
+    assert _lib.mlp_tp_attn_workspace_bytes(b, 0, h, a, d, 1) == 0     # s < 1
+    assert _lib.mlp_tp_attn_workspace_bytes(0, s, h, a, d, 1) == 0     # no tokens, nothing needed
+
+
+@pytest.mark.parametrize("b,s,h,a,d,t,code", [
+    (2, 64, 256, 2, 64, 1, "MLP_ESHAPE"),    # head width other than 128
+    (2, 64, 256, 3, 128, 2, "MLP_ESHAPE"),   # a % t
+    (2, 64, 250, 2, 128, 1, "MLP_ESHAPE"),   # h % 8
+    (2, 0, 256, 2, 128, 1, "MLP_EINVAL"),    # s < 1
+    (-1, 64, 256, 2, 128, 1, "MLP_EINVAL"),
+    (2, 64, 256, 2, 128, 0, "MLP_EINVAL"),
+])
+def test_attention_rejects_bad_shapes(L, b, s, h, a, d, t, code):
+    st = L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, b, s, h, a, d, t, 1, FAKE, FAKE, FAKE, FAKE, None)
+    assert st == _lib.STATUS_CODES[code]
+    st = L.mlp_tp_attn_backward(*([FAKE] * 7), b, s, h, a, d, t, 1, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == _lib.STATUS_CODES[code]
+
+
+def test_attention_rejects_null_misaligned_and_short_workspace(L):
+    shp = (2, 64, 256, 2, 128, 1, 1)
+    assert L.mlp_tp_attn_forward(None, FAKE, FAKE, *shp, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, *shp, FAKE + 8, FAKE, FAKE, FAKE, None) == 3
+    ws = _lib.mlp_tp_attn_workspace_bytes(2, 64, 256, 2, 128, 1)
+    args = [FAKE] * 7 + list(shp) + [FAKE] * 3
+    assert L.mlp_tp_attn_backward(*args, FAKE, ws - 256, None) == _lib.STATUS_CODES["MLP_EWORKSPACE"]
+    assert L.mlp_tp_attn_backward(*args, FAKE + 16, ws, None) == _lib.STATUS_CODES["MLP_EALIGN"]
+
+
+def test_recompute_backward_workspace_and_checks(L):
+    need = _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 2)
+    assert need >= _lib.mlp_tp_workspace_bytes(128, 64, 256, 2) + 128 * 256 * 2  # plus the recomputed G
+    assert _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 3) == 0
+    args = [FAKE] * 5 + [128, 64, 256, 2] + [FAKE] * 5
+    assert L.mlp_tp_backward_recompute(*args, FAKE, need - 256, None) == _lib.STATUS_CODES["MLP_EWORKSPACE"]
+    bad = [FAKE] * 5 + [128, 64, 256, 3] + [FAKE] * 5
+    assert L.mlp_tp_backward_recompute(*bad, FAKE, need, None) == _lib.STATUS_CODES["MLP_ESHAPE"]
