@@ -15,8 +15,8 @@
 //   warp 1     TMEM allocation and every tcgen05.mma: S_j = Q K_j^T into one of two TMEM
 //              S buffers, O += P_j V_j into the TMEM output accumulator
 //   warps 2-5  softmax, thread r <-> query row r (TMEM lane r): read S_j from TMEM, mask,
-//              running row max and sum (base 2), P_j -> shared memory (bf16, the A operand
-//              of the next MMA); rescale O in TMEM only when the row max has grown by more
+//              running row max and sum (base 2), P_j (bf16) back into TMEM over S_j, where
+//              the P_j V_j MMA reads it as its A operand; rescale O in TMEM only when the row max has grown by more
 //              than 2^8 since the last rescale (the final division by the row sum makes the
 //              result exact whatever reference the exponentials used). Finally C = O / l and
 //              the row's base-2 log-sum-exp L for the backward pass.
@@ -193,20 +193,23 @@ struct FwdCfg {
     static constexpr int THREADS = 192;
     static constexpr uint32_t QTILE = 128 * kHeadDim * 2;  // Q block: 32 KB
     static constexpr uint32_t KVTILE = 64 * kHeadDim * 2;  // K or V block: 16 KB
-    static constexpr uint32_t PTILE = 128 * 64 * 2;        // P block: 16 KB
     // K and V blocks have a ring of two slots each (slots 0-1 hold K, 2-3 hold V). A K slot is
     // freed as soon as its S MMA completes and a V slot when its PV MMA completes; the
     // producer issues K_0 K_1 and then V_j, K_{j+2} for each j, so a K load never queues
     // behind a V load that waits for a later PV.
-    static constexpr uint32_t OFF_Q = 0, OFF_KV = QTILE, OFF_P = QTILE + 4 * KVTILE, OFF_BAR = OFF_P + PTILE;
-    // barriers: q | full[4] | empty[4] | sfull[2] | sfree[2] | pfull | pvdone | drain
-    static constexpr int NUM_BARS = 1 + 8 + 4 + 3;
+    static constexpr uint32_t OFF_Q = 0, OFF_KV = QTILE, OFF_BAR = QTILE + 4 * KVTILE;
+    // barriers: q | full[4] | empty[4] | sfull[2] | pfull[2] | pvdone | drain. P_j's arrivals go
+    // to pfull[j % 2]: a softmax warp may run one block ahead of another (block j+1 needs only
+    // PV_{j-1}), and its arrival for j+1 must not complete block j's phase.
+    static constexpr int NUM_BARS = 1 + 8 + 2 + 2 + 2;
     // No alignment slack (two CTAs must fit in one SM's shared memory): the kernel checks
     // that its dynamic shared memory starts on a 1 KB boundary and otherwise does nothing.
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);
-    static constexpr uint32_t TMEM_COLS = 256;  // S[0] 0..63 | S[1] 64..127 | O 128..255
+    // S[0] 0..63 | S[1] 64..127 | O 128..255. P_j (bf16 pairs) overwrites the first 32 columns
+    // of S_j's buffer once the softmax has read S_j, and is the A operand of P_j V_j from there.
+    static constexpr uint32_t TMEM_COLS = 256;
     static constexpr uint32_t O_COL = 128;
     static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 };
@@ -221,10 +224,10 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
         return;
     }
     uint8_t* gbase = smem_raw;
-    const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV, sP = base + C::OFF_P;
+    const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 32, b_sf = b_empty + 32, b_sfree = b_sf + 16,
-                   b_pf = b_sfree + 16, b_pv = b_pf + 8, b_drain = b_pv + 8;
+    const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 32, b_sf = b_empty + 32, b_pf = b_sf + 16,
+                   b_pv = b_pf + 16, b_drain = b_pv + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -251,9 +254,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sf + 8 * i, 1);
-            mbar_init(b_sfree + 8 * i, 4);
+            mbar_init(b_pf + 8 * i, 4);
         }
-        mbar_init(b_pf, 4);
         mbar_init(b_pv, 1);
         mbar_init(b_drain, 1);
         *abort_flag = 0;
@@ -307,13 +309,14 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_q, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 1001, -1);
             bool any = false;
-            const uint64_t dQ = desc_k(sQ), dKV = desc_k(sKV), dP = desc_k(sP), dV = desc_mn(sKV, C::KVTILE / 2);
-            // S_j = Q K_j^T into TMEM score buffer j % 2
+            const uint64_t dQ = desc_k(sQ), dKV = desc_k(sKV), dV = desc_mn(sKV, C::KVTILE / 2);
+            // S_j = Q K_j^T into TMEM score buffer j % 2. For j >= 2 that buffer held P_{j-2}, the
+            // A operand of PV_{j-2}: that product must have completed first.
             auto issue_s = [&](int j) -> bool {
                 const int st = j & 1;
                 if (!mbar_wait_bounded(b_full + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
                                        DEV_TIMEOUT_MMA_FULL, 1002, j) ||
-                    (j >= 2 && !mbar_wait_bounded(b_sfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                    (j >= 2 && !mbar_wait_bounded(b_pv, (j - 2) & 1, abort_flag, args.status, limit,
                                                   DEV_TIMEOUT_MMA_ACC, 1003, j)))
                     return false;
                 tc_fence_after();
@@ -333,7 +336,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
             for (int j = 0; ok && j < 2 && j < nkb; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nkb; ++j) {  // O += P_j V_j
                 const int vs = 2 + (j & 1);
-                if (!mbar_wait_bounded(b_pf, j & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 1004, j) ||
+                if (!mbar_wait_bounded(b_pf + 8 * (j & 1), (j >> 1) & 1, abort_flag, args.status, limit,
+                                       DEV_TIMEOUT_MMA_ACC, 1004, j) ||
                     !mbar_wait_bounded(b_full + 8 * vs, (j >> 1) & 1, abort_flag, args.status, limit,
                                        DEV_TIMEOUT_MMA_FULL, 1005, j)) {
                     ok = false;
@@ -341,10 +345,11 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                 }
                 tc_fence_after();
                 const uint64_t dVs = desc_at(dV, vs * C::KVTILE);
+                // A = P_j in TMEM: 16 keys per MMA are 8 columns of bf16 pairs
 #pragma unroll
                 for (int k = 0; k < C::BKV / 16; ++k)
-                    umma_bf16(tmem + C::O_COL, desc_at(dP, 32u * k), desc_at(dVs, 2048u * k), C::IDESC_PV,
-                              (j > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + C::O_COL, tmem + 64u * (j & 1) + 8u * k, desc_at(dVs, 2048u * k),
+                                     C::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(b_pv);
                 umma_commit(b_empty + 8 * vs);
                 if (j + 2 < nkb) ok = issue_s(j + 2);
@@ -380,9 +385,6 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                     x[32 + i] = __uint_as_float(u1[i]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_sfree + 8 * st);
             const int k0 = j * C::BKV;
             if ((args.causal && k0 + C::BKV - 1 > q0) || k0 + C::BKV > s) {  // CTA-uniform
 #pragma unroll
@@ -403,13 +405,13 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 64; ++c) x[c] = ex2(fmaf(x[c], c2, nref));
             l += sum_tree(x);
-            // P (single buffer) and O are free to touch once PV_{j-1} has completed
-            if (j >= 1) {
+            // O may be rescaled once PV_{j-1} has completed (only when some row's max grew)
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {
                 if (!warp_wait(b_pv, (j - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1007, j)) {
                     ok = false;
                     break;
                 }
-                if (__any_sync(0xffffffffu, resc)) {  // rescale the O row in place
+                {
                     tc_fence_after();
                     uint32_t o[32];
 #pragma unroll 1
@@ -424,12 +426,23 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                     tmem_st_wait();
                 }
             }
-            store_row_sw128<64, C::BQ>(sP, r, x);
-            fence_proxy_async_smem();
+            {  // P_j as bf16 pairs over the first 32 columns of S_j's buffer (read above)
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack2_bf16(x[2 * i], x[2 * i + 1]);
+                tmem_st_32x32b_x32(t_lane + 64u * st, pk);
+                tmem_st_wait();
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_pf);
+            if (lane == 0) mbar_arrive(b_pf + 8 * st);
         }
+        // O is final once PV_{nkb-1} has completed. A warp that ran ahead may find the PV
+        // barrier two phases behind (its last S only implies PV_{nkb-3}), where a parity wait
+        // for phase nkb-1 would match the completed phase nkb-3: wait for nkb-2 first.
+        if (ok && nkb > 1 &&
+            !warp_wait(b_pv, (nkb - 2) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1008, nkb))
+            ok = false;
         if (ok && nkb > 0 &&
             warp_wait(b_pv, (nkb - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
             tc_fence_after();
