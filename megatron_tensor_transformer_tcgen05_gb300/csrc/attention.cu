@@ -25,7 +25,7 @@
 //     blocks: S^T = K Q^T, dP^T = V dC^T, P^T = exp2(S^T c - L), dS^T = P^T (dP^T - D),
 //     dV += P^T dC, dK += dS^T Q.
 //   attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query block), looping over 64-key
-//     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D), dQ += dS K.
+//     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D) (back into TMEM over S), dQ += dS K.
 //   with D = rowsum(dC * C) from attn_bwd_dot_kernel.
 // A tile of Q, K, V or dC is loaded once, row-major with a 128-byte swizzle, and read by
 // the tensor core both as a K-major operand (contraction over d) and as an MN-major one
@@ -736,15 +736,16 @@ struct DqCfg {
     static constexpr int STAGES = 4;                    // K / V blocks in flight
     static constexpr uint32_t QT = 128 * kHeadDim * 2;  // Q or dC block: 32 KB
     static constexpr uint32_t KT = 64 * kHeadDim * 2;   // K or V block: 16 KB
-    static constexpr uint32_t ST = 128 * 64 * 2;        // dS block: 16 KB
-    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_KV = 2 * QT, OFF_DS = 2 * QT + STAGES * 2 * KT,
-                              OFF_BAR = OFF_DS + 2 * ST;
-    // barriers: qdo | kvfull[4] | kvempty[4] | spfull[2] | spfree[2] | dsfull[2] | dsfree[2] | dqfull | drain
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 8 + 2;
+    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_KV = 2 * QT, OFF_BAR = 2 * QT + STAGES * 2 * KT;
+    // barriers: qdo | kvfull[4] | kvempty[4] | spfull[2] | dsfull[2] | dqdone[2] | dqfull | drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 6 + 2;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 128, false, true);
-    static constexpr uint32_t TMEM_COLS = 512;  // S[x] at 128x, dP[x] at 128x + 64; dQ at 256
+    // S[x] at 128x, dP[x] at 128x + 64; dQ at 256. dS_j (bf16 pairs) is written back over the
+    // S_j columns each thread has read (keys [32h, 32h+32) at 128x + 32h) and is the A operand
+    // of dQ += dS_j K_j from there.
+    static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DQ_COL = 256;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -756,11 +757,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sKV = base + C::OFF_KV, sdS = base + C::OFF_DS;
+    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sKV = base + C::OFF_KV;
     const uint32_t bar = base + C::OFF_BAR;
     const uint32_t b_qdo = bar, b_kvf = bar + 8, b_kve = b_kvf + 8 * C::STAGES, b_spf = b_kve + 8 * C::STAGES,
-                   b_spfree = b_spf + 16, b_dsf = b_spfree + 16, b_dsfree = b_dsf + 16, b_dq = b_dsfree + 16,
-                   b_drain = b_dq + 8;
+                   b_dsf = b_spf + 16, b_dqd = b_dsf + 16, b_dq = b_dqd + 16, b_drain = b_dq + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -786,9 +786,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_spf + 8 * i, 1);
-            mbar_init(b_spfree + 8 * i, 8);
             mbar_init(b_dsf + 8 * i, 8);
-            mbar_init(b_dsfree + 8 * i, 1);
+            mbar_init(b_dqd + 8 * i, 1);
         }
         mbar_init(b_dq, 1);
         mbar_init(b_drain, 1);
@@ -840,14 +839,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_qdo, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 2001, -1);
             bool any = false;
-            const uint64_t dQ = desc_k(sQ), dO = desc_k(sdO), dKV = desc_k(sKV), dKmn = desc_mn(sKV, C::KT / 2),
-                           dS = desc_k(sdS);
+            const uint64_t dQ = desc_k(sQ), dO = desc_k(sdO), dKV = desc_k(sKV), dKmn = desc_mn(sKV, C::KT / 2);
             for (int j = 0; ok && j <= nkb; ++j) {
                 if (j < nkb) {  // S_j = Q K_j^T, dP_j = dC V_j^T
                     const int st = j & 1, ks = j % C::STAGES;
                     if (!mbar_wait_bounded(b_kvf + 8 * ks, (j / C::STAGES) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 2002, j) ||
-                        (j >= 2 && !mbar_wait_bounded(b_spfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
+                        // the buffer held dS_{j-2}, the A operand of dQ_{j-2}
+                        (j >= 2 && !mbar_wait_bounded(b_dqd + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
                                                       limit, DEV_TIMEOUT_MMA_ACC, 2003, j))) {
                         ok = false;
                         break;
@@ -872,13 +871,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dsoff = pst * C::ST, koff = ks * 2 * C::KT;
+                    const uint32_t koff = ks * 2 * C::KT;
+                    // A = dS_{pj} in TMEM: keys [16k, 16k+16) are 8 columns at 128 pst + 32 (k / 2) + 8 (k % 2)
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k)
-                        umma_bf16(tmem + C::DQ_COL, desc_at(dS, dsoff + 32u * k), desc_at(dKmn, koff + 2048u * k),
-                                  C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16_tmem_a(tmem + C::DQ_COL, tmem + 128u * pst + 32u * (k >> 1) + 8u * (k & 1),
+                                         desc_at(dKmn, koff + 2048u * k), C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
                     umma_commit(b_kve + 8 * ks);
-                    umma_commit(b_dsfree + 8 * pst);
+                    umma_commit(b_dqd + 8 * pst);
                 }
             }
             if (ok && any) umma_commit(b_dq);
@@ -915,9 +915,6 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                     dp[e] = __uint_as_float(u1[e]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_spfree + 8 * st);
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
 #pragma unroll
@@ -929,14 +926,13 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                 }
                 dp[c] = pv * (dp[c] - Dq);
             }
-            // the dS buffer is free once dQ_{j-2} has completed
-            if (j >= 2 && !warp_wait(b_dsfree + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
-                                     DEV_TIMEOUT_EPILOGUE, 2006, j)) {
-                ok = false;
-                break;
+            {  // dS over the first 16 of the 32 S columns this thread has read
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack2_bf16(dp[2 * i], dp[2 * i + 1]);
+                tmem_st_32x32b_x16(t_lane + 128u * st + cb, pk);
+                tmem_st_wait();
             }
-            store_row_part_sw128<32, C::BQ>(sdS + st * C::ST, r, cb, dp);
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dsf + 8 * st);
