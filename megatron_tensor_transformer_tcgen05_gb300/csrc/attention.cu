@@ -22,8 +22,8 @@
 //              the row's base-2 log-sum-exp L for the backward pass.
 // Backward, deterministic (no atomics), two kernels that each recompute P from Q, K and L:
 //   attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key block), looping over 64-query
-//     blocks: S^T = K Q^T, dP^T = V dC^T, P^T = exp2(S^T c - L), dS^T = P^T (dP^T - D),
-//     dV += P^T dC, dK += dS^T Q.
+//     blocks: S^T = K Q^T, dP^T = V dC^T, P^T = exp2(S^T c - L), dS^T = P^T (dP^T - D) (both
+//     back into TMEM over S^T and dP^T), dV += P^T dC, dK += dS^T Q.
 //   attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query block), looping over 64-key
 //     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D) (back into TMEM over S), dQ += dS K.
 //   with D = rowsum(dC * C) from attn_bwd_dot_kernel.
@@ -50,11 +50,6 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 __device__ __forceinline__ float4 lds128f(uint32_t addr)
 {
     float4 v;
@@ -69,37 +64,6 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Row r of a K-major, 128-byte-swizzled bf16 operand tile with ROWS rows: columns
-// [64k, 64k+64) form chunk k (ROWS x 128 bytes); 16-byte unit u of a row sits at unit
-// u ^ (r % 8), the layout a TMA SWIZZLE_128B load produces and the descriptors expect.
-template <int NCOLS, int ROWS>
-__device__ __forceinline__ void store_row_sw128(uint32_t buf, int r, const float (&v)[NCOLS])
-{
-#pragma unroll
-    for (int kc = 0; kc < NCOLS / 64; ++kc)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = 64 * kc + 8 * u;
-            sts128(buf + static_cast<uint32_t>(kc * ROWS * 128 + r * 128) + ((static_cast<uint32_t>(u) ^ (r & 7)) << 4),
-                   pack2_bf16(v[c], v[c + 1]), pack2_bf16(v[c + 2], v[c + 3]), pack2_bf16(v[c + 4], v[c + 5]),
-                   pack2_bf16(v[c + 6], v[c + 7]));
-        }
-}
-
-// Columns [c0, c0 + NC) of row r of the same layout (c0 a multiple of 8).
-template <int NC, int ROWS>
-__device__ __forceinline__ void store_row_part_sw128(uint32_t buf, int r, int c0, const float (&v)[NC])
-{
-#pragma unroll
-    for (int i = 0; i < NC / 8; ++i) {
-        const int c = c0 + 8 * i;
-        const uint32_t kc = static_cast<uint32_t>(c >> 6), u = static_cast<uint32_t>((c >> 3) & 7);
-        sts128(buf + kc * (ROWS * 128u) + static_cast<uint32_t>(r * 128) + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
-               pack2_bf16(v[8 * i], v[8 * i + 1]), pack2_bf16(v[8 * i + 2], v[8 * i + 3]),
-               pack2_bf16(v[8 * i + 4], v[8 * i + 5]), pack2_bf16(v[8 * i + 6], v[8 * i + 7]));
-    }
 }
 
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v)
@@ -198,10 +162,11 @@ struct FwdCfg {
     // producer issues K_0 K_1 and then V_j, K_{j+2} for each j, so a K load never queues
     // behind a V load that waits for a later PV.
     static constexpr uint32_t OFF_Q = 0, OFF_KV = QTILE, OFF_BAR = QTILE + 4 * KVTILE;
-    // barriers: q | full[4] | empty[4] | sfull[2] | pfull[2] | pvdone | drain. P_j's arrivals go
-    // to pfull[j % 2]: a softmax warp may run one block ahead of another (block j+1 needs only
-    // PV_{j-1}), and its arrival for j+1 must not complete block j's phase.
-    static constexpr int NUM_BARS = 1 + 8 + 2 + 2 + 2;
+    // barriers: q | full[4] | empty[4] | sfull[2] | pfull[2] | pvdone[2] | drain. Everything that
+    // alternates between the two score buffers has a barrier per buffer (P_j V_j completes
+    // pvdone[j % 2]): a softmax warp may run one block ahead of another, and a parity wait is
+    // only sound while its barrier is at most one phase from the phase waited for.
+    static constexpr int NUM_BARS = 1 + 8 + 2 + 2 + 2 + 1;
     // No alignment slack (two CTAs must fit in one SM's shared memory): the kernel checks
     // that its dynamic shared memory starts on a 1 KB boundary and otherwise does nothing.
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NUM_BARS + 16;
@@ -227,7 +192,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
     const uint32_t sQ = base + C::OFF_Q, sKV = base + C::OFF_KV;
     const uint32_t bar = base + C::OFF_BAR;
     const uint32_t b_q = bar, b_full = bar + 8, b_empty = b_full + 32, b_sf = b_empty + 32, b_pf = b_sf + 16,
-                   b_pv = b_pf + 16, b_drain = b_pv + 8;
+                   b_pv = b_pf + 16, b_drain = b_pv + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -255,8 +220,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sf + 8 * i, 1);
             mbar_init(b_pf + 8 * i, 4);
+            mbar_init(b_pv + 8 * i, 1);
         }
-        mbar_init(b_pv, 1);
         mbar_init(b_drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -316,7 +281,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                 const int st = j & 1;
                 if (!mbar_wait_bounded(b_full + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit,
                                        DEV_TIMEOUT_MMA_FULL, 1002, j) ||
-                    (j >= 2 && !mbar_wait_bounded(b_pv, (j - 2) & 1, abort_flag, args.status, limit,
+                    (j >= 2 && !mbar_wait_bounded(b_pv + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
                                                   DEV_TIMEOUT_MMA_ACC, 1003, j)))
                     return false;
                 tc_fence_after();
@@ -350,7 +315,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                 for (int k = 0; k < C::BKV / 16; ++k)
                     umma_bf16_tmem_a(tmem + C::O_COL, tmem + 64u * (j & 1) + 8u * k, desc_at(dVs, 2048u * k),
                                      C::IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(b_pv);
+                umma_commit(b_pv + 8 * (j & 1));
                 umma_commit(b_empty + 8 * vs);
                 if (j + 2 < nkb) ok = issue_s(j + 2);
             }
@@ -407,7 +372,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
             l += sum_tree(x);
             // O may be rescaled once PV_{j-1} has completed (only when some row's max grew)
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-                if (!warp_wait(b_pv, (j - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1007, j)) {
+                if (!warp_wait(b_pv + 8 * (st ^ 1), ((j - 1) >> 1) & 1, abort_flag, args.status, limit,
+                               DEV_TIMEOUT_EPILOGUE, 1007, j)) {
                     ok = false;
                     break;
                 }
@@ -437,14 +403,16 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(b_pf + 8 * st);
         }
-        // O is final once PV_{nkb-1} has completed. A warp that ran ahead may find the PV
-        // barrier two phases behind (its last S only implies PV_{nkb-3}), where a parity wait
-        // for phase nkb-1 would match the completed phase nkb-3: wait for nkb-2 first.
-        if (ok && nkb > 1 &&
-            !warp_wait(b_pv, (nkb - 2) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1008, nkb))
+        // O is final once PV_{nkb-2} and PV_{nkb-1} have completed (a warp's last S implies only
+        // PV_{nkb-3}); each waits on its own buffer's barrier, whose next phase never comes.
+        const int l1 = nkb - 1, l2 = nkb - 2;
+        if (ok && l2 >= 0 &&
+            !warp_wait(b_pv + 8 * (l2 & 1), (l2 >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1008,
+                       nkb))
             ok = false;
-        if (ok && nkb > 0 &&
-            warp_wait(b_pv, (nkb - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1009, nkb)) {
+        if (ok && l1 >= 0 &&
+            warp_wait(b_pv + 8 * (l1 & 1), (l1 >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 1009,
+                      nkb)) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * hd + colQ;
@@ -470,18 +438,20 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
 struct DkdvCfg {
     static constexpr int BKV = 128, BQ = 64;
     static constexpr int THREADS = 320;  // producer, MMA, 8 element-wise warps (two threads per key)
-    static constexpr int STAGES = 3;                    // Q / dC blocks in flight
+    static constexpr int STAGES = 4;                    // Q / dC blocks in flight
     static constexpr uint32_t KT = 128 * kHeadDim * 2;  // K or V block: 32 KB
     static constexpr uint32_t QT = 64 * kHeadDim * 2;   // Q or dC block: 16 KB
-    static constexpr uint32_t PT = 128 * 64 * 2;        // P^T or dS^T block: 16 KB
-    static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_QD = 2 * KT, OFF_P = 2 * KT + STAGES * 2 * QT,
-                              OFF_DS = OFF_P + PT, OFF_LD = OFF_DS + PT, OFF_BAR = OFF_LD + 8 * 2 * 32 * 4;
-    // barriers: kv | qdofull[3] | qdoempty[3] | stfull[2] | stfree[2] | pdfull | pdfree | accfull | drain
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 4 + 4;
+    static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_QD = 2 * KT, OFF_LD = 2 * KT + STAGES * 2 * QT,
+                              OFF_BAR = OFF_LD + 8 * 2 * 32 * 4;
+    // barriers: kv | qdofull[4] | qdoempty[4] | stfull[2] | pdfull[2] | dvdkdone[2] | accfull | drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 6 + 2;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, 128, false, true);
-    static constexpr uint32_t TMEM_COLS = 512;  // S^T[x] at 128x, dP^T[x] at 128x + 64; dV 256; dK 384
+    // S^T[x] at 128x, dP^T[x] at 128x + 64; dV 256; dK 384. P^T and dS^T (bf16 pairs) are
+    // written back over the S^T and dP^T columns each thread has read (queries [32h, 32h+32) at
+    // +32h) and are the A operands of dV += P^T dC and dK += dS^T Q from there.
+    static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DV_COL = 256, DK_COL = 384;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -493,12 +463,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQD = base + C::OFF_QD, sP = base + C::OFF_P,
-                   sdS = base + C::OFF_DS, sLD = base + C::OFF_LD;
+    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQD = base + C::OFF_QD, sLD = base + C::OFF_LD;
     const uint32_t bar = base + C::OFF_BAR;
     const uint32_t b_kv = bar, b_qf = bar + 8, b_qe = b_qf + 8 * C::STAGES, b_stf = b_qe + 8 * C::STAGES,
-                   b_stfree = b_stf + 16, b_pdf = b_stfree + 16, b_pdfree = b_pdf + 8, b_acc = b_pdfree + 8,
-                   b_drain = b_acc + 8;
+                   b_pdf = b_stf + 16, b_dvd = b_pdf + 16, b_acc = b_dvd + 16, b_drain = b_acc + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -526,10 +494,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_stf + 8 * i, 1);
-            mbar_init(b_stfree + 8 * i, 8);
+            mbar_init(b_pdf + 8 * i, 8);
+            mbar_init(b_dvd + 8 * i, 1);
         }
-        mbar_init(b_pdf, 8);
-        mbar_init(b_pdfree, 1);
         mbar_init(b_acc, 1);
         mbar_init(b_drain, 1);
         *abort_flag = 0;
@@ -581,14 +548,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_kv, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 3001, -1);
             bool any = false;
-            const uint64_t dK = desc_k(sK), dV = desc_k(sV), dQD = desc_k(sQD), dQDmn = desc_mn(sQD, C::QT / 2),
-                           dP = desc_k(sP), dS = desc_k(sdS);
+            const uint64_t dK = desc_k(sK), dV = desc_k(sV), dQD = desc_k(sQD), dQDmn = desc_mn(sQD, C::QT / 2);
             for (int i = 0; ok && i <= nq; ++i) {
                 if (i < nq) {  // S^T_i = K Q_i^T, dP^T_i = V dC_i^T
                     const int st = i & 1, qs = i % C::STAGES;
                     if (!mbar_wait_bounded(b_qf + 8 * qs, (i / C::STAGES) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 3002, i) ||
-                        (i >= 2 && !mbar_wait_bounded(b_stfree + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status,
+                        // the buffer held P^T_{i-2} and dS^T_{i-2}, the A operands of dV / dK of block i-2
+                        (i >= 2 && !mbar_wait_bounded(b_dvd + 8 * st, ((i - 2) >> 1) & 1, abort_flag, args.status,
                                                       limit, DEV_TIMEOUT_MMA_ACC, 3003, i))) {
                         ok = false;
                         break;
@@ -607,24 +574,25 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     umma_commit(b_stf + 8 * st);
                 }
                 if (i >= 1) {  // dV += P^T_{i-1} dC_{i-1}, dK += dS^T_{i-1} Q_{i-1}
-                    const int pi = i - 1, qs = pi % C::STAGES;
-                    if (!mbar_wait_bounded(b_pdf, pi & 1, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_ACC, 3004,
-                                           pi)) {
+                    const int pi = i - 1, qs = pi % C::STAGES, pst = pi & 1;
+                    if (!mbar_wait_bounded(b_pdf + 8 * pst, (pi >> 1) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_ACC, 3004, pi)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t qoff = qs * 2 * C::QT, dooff = qoff + C::QT;
+                    // A = P^T and dS^T in TMEM: queries [16k, 16k+16) are 8 columns at +32 (k / 2) + 8 (k % 2)
 #pragma unroll
                     for (int k = 0; k < C::BQ / 16; ++k) {
                         const uint32_t acc = (pi > 0 || k > 0) ? 1u : 0u;
-                        umma_bf16(tmem + C::DV_COL, desc_at(dP, 32u * k), desc_at(dQDmn, dooff + 2048u * k), C::IDESC_ACC,
-                                  acc);
-                        umma_bf16(tmem + C::DK_COL, desc_at(dS, 32u * k), desc_at(dQDmn, qoff + 2048u * k), C::IDESC_ACC,
-                                  acc);
+                        const uint32_t pa = tmem + 128u * pst + 32u * (k >> 1) + 8u * (k & 1);
+                        umma_bf16_tmem_a(tmem + C::DV_COL, pa, desc_at(dQDmn, dooff + 2048u * k), C::IDESC_ACC, acc);
+                        umma_bf16_tmem_a(tmem + C::DK_COL, pa + 64u, desc_at(dQDmn, qoff + 2048u * k), C::IDESC_ACC,
+                                         acc);
                     }
                     umma_commit(b_qe + 8 * qs);
-                    umma_commit(b_pdfree);
+                    umma_commit(b_dvd + 8 * pst);
                 }
             }
             if (ok && any) umma_commit(b_acc);
@@ -671,9 +639,6 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     dp[e] = __uint_as_float(u1[e]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_stfree + 8 * st);
             const int blk0 = (qb_first + i) * C::BQ;
             const bool need_mask = (args.causal && blk0 < k0 + C::BKV - 1) || blk0 + C::BQ > s || k0 + C::BKV > s;
 #pragma unroll
@@ -692,18 +657,20 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     dp[c] = pv * (dp[c] - Dv[e]);
                 }
             }
-            // the single P^T / dS^T buffer is free once the dV / dK MMAs of block i-1 completed
-            if (i >= 1 && !warp_wait(b_pdfree, (i - 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE,
-                                     3006, i)) {
-                ok = false;
-                break;
+            {  // P^T and dS^T over the first 16 of the 32 S^T / dP^T columns this thread has read
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack2_bf16(p[2 * e], p[2 * e + 1]);
+                    dk[e] = pack2_bf16(dp[2 * e], dp[2 * e + 1]);
+                }
+                tmem_st_32x32b_x16(t_lane + 128u * st + cb, pk);
+                tmem_st_32x32b_x16(t_lane + 128u * st + 64u + cb, dk);
+                tmem_st_wait();
             }
-            store_row_part_sw128<32, C::BKV>(sP, r, cb, p);
-            store_row_part_sw128<32, C::BKV>(sdS, r, cb, dp);
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_pdf);
+            if (lane == 0) mbar_arrive(b_pdf + 8 * st);
         }
         if (ok && nq > 0 && warp_wait(b_acc, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3007, -1)) {
             tc_fence_after();
