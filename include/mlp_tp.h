@@ -27,6 +27,17 @@
  * Ownership: the caller allocates every buffer (device memory) and owns the stream; the
  * library allocates no device memory and keeps no pointer after a call returns.
  *
+ * Split tails (all GEMMs whose output is the accumulator, or the accumulator plus a bias):
+ * a GEMM of tiles tiles on u units (CTA pairs, or CTAs) runs them in rounds of u; when
+ * tiles % u leaves the last round short, the call may cut each of those last tiles into
+ * S >= 2 ranges of K (each at least 16 k blocks of 64, S * (tiles % u) <= u) that run side
+ * by side. Each range writes its fp32 partial tile to the workspace, and one more launch
+ * adds a tile's S partials in range order (then the bias) and rounds once to bf16. This
+ * needs workspace room (at most mlp_tp_forward_workspace_bytes(), which every backward
+ * workspace size below includes); the forward entry points take it as an optional
+ * argument and, without it, run every tile whole. The sum order is fixed by the sizes and
+ * the device's SM count, so results stay bitwise reproducible run to run.
+ *
  * Execution: calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = the legacy
  * default stream) of the current device. All arguments are checked before anything is
  * launched; a failing check returns its status and launches nothing. Launch failures
@@ -68,10 +79,19 @@ typedef uint16_t mlp_bf16;
  * then Y = G*B + b (second GEMM; its K loop runs over the t shards' row blocks of B into
  * one accumulator, so the shard sum never leaves the chip). H and G are the activations
  * the backward needs ("Distributed training", section 2.2: the MLP keeps the GELU input
- * and the down-projection input). Two kernel launches. */
+ * and the down-projection input). Two kernel launches, plus one when the second GEMM's
+ * tail is split. `workspace` is optional (NULL, or device memory 256-byte aligned, else
+ * MLP_EALIGN): room for the split tail's partial tiles, used up to workspace_bytes
+ * (mlp_tp_forward_workspace_bytes() is always enough); its contents on entry do not
+ * matter. */
 mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
                           const mlp_bf16* B, const mlp_bf16* b, int T, int h, int f, int t,
-                          mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* cuda_stream);
+                          mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* workspace,
+                          size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes with which every forward entry point (mlp_tp_forward,
+ * mlp_tp_swiglu_forward, mlp_tp_attn_forward) splits every tail it can: 40 MiB. */
+size_t mlp_tp_forward_workspace_bytes(void);
 
 /* Forward pass followed by the block's fused output step ("Efficient Large-Scale Language
  * Model Training on GPU Clusters Using Megatron-LM", section 3, "Fused element-wise
@@ -102,8 +122,10 @@ mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, u
  *   da = colsum(dH) (fp32; the dH GEMM sums its fp32 dH over 32-row blocks in the
  *        epilogue),  db = colsum(dY) (fp32)
  * `workspace` (device, >= mlp_tp_workspace_bytes(T,h,f,t) bytes, 256-byte aligned) holds
- * dH and the reduction partials; its contents on entry do not matter. On return its first
- * T*f*2 bytes hold dH = dL/dH (row-major bf16 [T,f]). Six launches. */
+ * dH, the reduction partials and the split tails' parts; its contents on entry do not
+ * matter. On return its first
+ * T*f*2 bytes hold dH = dL/dH (row-major bf16 [T,f]). Six launches, plus one for each of
+ * the dX, dA and dB GEMMs whose tail is split. */
 mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
                            const mlp_bf16* H, const mlp_bf16* G, const mlp_bf16* dY,
                            int T, int h, int f, int t,
@@ -136,15 +158,18 @@ mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf16* dY, int
  *   X [T,h]  A, Wg [h,f]  B [f,h]  Ha, Hg, U [T,f]  Y [T,h]
  * Forward: Ha = X A and Hg = X Wg come out of one GEMM (both halves of one 256-wide MMA per
  * 128 output columns, sharing the X tiles) whose epilogue also writes U = SiLU(Ha) Hg; then
- * Y = U B. Ha, Hg, U are kept for the backward. Two launches. */
+ * Y = U B. Ha, Hg, U are kept for the backward. Two launches (plus one when Y's GEMM tail
+ * is split; `workspace` is optional, as for mlp_tp_forward). */
 mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
                                  const mlp_bf16* B, int T, int h, int f, int t, mlp_bf16* Ha,
-                                 mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* cuda_stream);
+                                 mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* workspace,
+                                 size_t workspace_bytes, void* cuda_stream);
 
 /* SwiGLU backward given dY: dU = dY B^T; dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha) (in the
  * dU GEMM's epilogue); dX = dHa A^T + dHg Wg^T (one accumulator over both K segments);
  * dA = X^T dHa; dWg = X^T dHg; dB = U^T dY. `workspace` (>= mlp_tp_swiglu_workspace_bytes(),
- * 256-byte aligned) holds dHa and dHg. Five launches. */
+ * 256-byte aligned) holds dHa and dHg, then the split tails' parts. Five launches, plus
+ * one per split tail. */
 mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
                                   const mlp_bf16* B, const mlp_bf16* Ha, const mlp_bf16* Hg,
                                   const mlp_bf16* U, const mlp_bf16* dY, int T, int h, int f, int t,
@@ -165,7 +190,7 @@ size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
  * anyway) into the workspace, and dB = G^T dY reads it there. dX, dA, da and db are bitwise
  * those of mlp_tp_backward; dB differs only by G being recomputed from the rounded H.
  * Workspace (256-byte aligned, at least mlp_tp_recompute_workspace_bytes): dH [T,f] bf16 |
- * G [T,f] bf16 | the reduction partials; dH and G are there on return. Other arguments and
+ * G [T,f] bf16 | the reduction partials | split-tail parts; dH and G are there on return. Other arguments and
  * errors as mlp_tp_backward. */
 size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t);
 mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
@@ -188,9 +213,10 @@ int mlp_tp_last_device_where(int* block, int* thread, int* tile, int* kblock);
 /* Human-readable name of a status. Never NULL. */
 const char* mlp_tp_status_string(mlp_status s);
 
-/* Number of kernel launches one mlp_tp_forward / mlp_tp_backward call makes for these sizes
- * (the attention block's calls make 3 and 7). */
-int mlp_tp_launches_per_call(int backward, int T);
+/* Kernel launches the library has made since it was loaded (every entry point, device and
+ * stream): the difference across a region counts the region's launches, split-tail fixups
+ * included. */
+long long mlp_tp_launch_count(void);
 
 /* Self-test of the bounded-wait path: launches one small kernel that waits on a barrier
  * nothing will ever complete, with a limit of `limit_ns` nanoseconds; the wait runs out,
@@ -255,13 +281,15 @@ const char* mlp_tp_kernel_name(int kernel);
  * Shapes: b >= 0, s >= 1, h >= 8 and h % 8 == 0, a >= 1, d == 128 (the one head width the
  * kernels are written for; MLP_ESHAPE otherwise), t >= 1 with a % t == 0. Pointers as for
  * the MLP block (token-indexed ones may be NULL when b == 0). Results are bitwise
- * reproducible run to run (no atomics anywhere). */
+ * reproducible run to run (no atomics anywhere). Three launches, plus one per split GEMM
+ * tail; `workspace` is optional, as for mlp_tp_forward. */
 mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo, int b, int s, int h,
                                int a, int d, int t, int causal, mlp_bf16* QKV, mlp_bf16* C, float* L, mlp_bf16* Y,
-                               void* cuda_stream);
+                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Device workspace mlp_tp_attn_backward needs (bytes; 0 for inadmissible shapes):
- * dC [T, a*d] bf16 | D [b*a, s] fp32 | dQKV [T, 3*a*d] bf16, each 256-byte aligned. */
+ * dC [T, a*d] bf16 | D [b*a, s] fp32 | dQKV [T, 3*a*d] bf16 | split-tail parts, each
+ * 256-byte aligned. */
 size_t mlp_tp_attn_workspace_bytes(int b, int s, int h, int a, int d, int t);
 
 /* Backward of the attention block given dY and the forward's QKV, C and L:

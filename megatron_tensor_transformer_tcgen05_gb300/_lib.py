@@ -48,7 +48,9 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             vp, i32, sz, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_ulonglong
             L.mlp_tp_forward.restype = i32
-            L.mlp_tp_forward.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 3 + [vp]
+            L.mlp_tp_forward.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 3 + [vp, sz, vp]
+            L.mlp_tp_forward_workspace_bytes.restype = sz
+            L.mlp_tp_forward_workspace_bytes.argtypes = []
             L.mlp_tp_backward.restype = i32
             L.mlp_tp_backward.argtypes = [vp] * 6 + [i32] * 4 + [vp] * 5 + [vp, sz, vp]
             L.mlp_tp_workspace_bytes.restype = sz
@@ -61,8 +63,8 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_last_device_where.argtypes = [vp, vp, vp, vp]
             L.mlp_tp_status_string.restype = ctypes.c_char_p
             L.mlp_tp_status_string.argtypes = [i32]
-            L.mlp_tp_launches_per_call.restype = i32
-            L.mlp_tp_launches_per_call.argtypes = [i32, i32]
+            L.mlp_tp_launch_count.restype = ctypes.c_longlong
+            L.mlp_tp_launch_count.argtypes = []
             L.mlp_tp_selftest_wait_timeout.restype = i32
             L.mlp_tp_selftest_wait_timeout.argtypes = [u64, vp]
             L.mlp_tp_timing_enable.restype = i32
@@ -77,7 +79,7 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_dropout_backward.restype = i32
             L.mlp_tp_dropout_backward.argtypes = [vp, i32, i32, ctypes.c_double, u64, u64, vp, vp]
             L.mlp_tp_swiglu_forward.restype = i32
-            L.mlp_tp_swiglu_forward.argtypes = [vp] * 4 + [i32] * 4 + [vp] * 4 + [vp]
+            L.mlp_tp_swiglu_forward.argtypes = [vp] * 4 + [i32] * 4 + [vp] * 4 + [vp, sz, vp]
             L.mlp_tp_swiglu_backward.restype = i32
             L.mlp_tp_swiglu_backward.argtypes = [vp] * 8 + [i32] * 4 + [vp] * 5 + [sz, vp]
             L.mlp_tp_swiglu_workspace_bytes.restype = sz
@@ -85,7 +87,7 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_bias_grads_noalloc.restype = i32
             L.mlp_tp_bias_grads_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
             L.mlp_tp_attn_forward.restype = i32
-            L.mlp_tp_attn_forward.argtypes = [vp] * 3 + [i32] * 7 + [vp] * 4 + [vp]
+            L.mlp_tp_attn_forward.argtypes = [vp] * 3 + [i32] * 7 + [vp] * 4 + [vp, sz, vp]
             L.mlp_tp_attn_workspace_bytes.restype = sz
             L.mlp_tp_attn_workspace_bytes.argtypes = [i32] * 6
             L.mlp_tp_attn_backward.restype = i32
@@ -120,9 +122,15 @@ def _check(status: int, where: str) -> None:
         raise MlpError(status, where)
 
 
-def mlp_tp_forward(X, A, a, B, b, T: int, h: int, f: int, t: int, H, G, Y, stream=None) -> None:
+def mlp_tp_forward(X, A, a, B, b, T: int, h: int, f: int, t: int, H, G, Y, workspace, workspace_bytes: int,
+                   stream=None) -> None:
     _check(lib().mlp_tp_forward(_ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), T, h, f, t,
-                                _ptr(H), _ptr(G), _ptr(Y), _stream(stream)), "mlp_tp_forward")
+                                _ptr(H), _ptr(G), _ptr(Y), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mlp_tp_forward")
+
+
+def mlp_tp_forward_workspace_bytes() -> int:
+    return int(lib().mlp_tp_forward_workspace_bytes())
 
 
 def mlp_tp_backward(X, A, B, H, G, dY, T: int, h: int, f: int, t: int, dX, dA, dB, da, db,
@@ -157,8 +165,8 @@ def mlp_tp_status_string(status: int) -> str:
     return lib().mlp_tp_status_string(status).decode()
 
 
-def mlp_tp_launches_per_call(backward: bool, T: int) -> int:
-    return int(lib().mlp_tp_launches_per_call(int(bool(backward)), T))
+def mlp_tp_launch_count() -> int:
+    return int(lib().mlp_tp_launch_count())
 
 
 def mlp_tp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
@@ -203,9 +211,11 @@ def mlp_tp_dropout_backward(dZ, T: int, h: int, p: float, seed: int, offset: int
                                          _stream(stream)), "mlp_tp_dropout_backward")
 
 
-def mlp_tp_swiglu_forward(X, A, Wg, B, T: int, h: int, f: int, t: int, Ha, Hg, U, Y, stream=None) -> None:
+def mlp_tp_swiglu_forward(X, A, Wg, B, T: int, h: int, f: int, t: int, Ha, Hg, U, Y, workspace, workspace_bytes: int,
+                          stream=None) -> None:
     _check(lib().mlp_tp_swiglu_forward(_ptr(X), _ptr(A), _ptr(Wg), _ptr(B), T, h, f, t, _ptr(Ha), _ptr(Hg),
-                                       _ptr(U), _ptr(Y), _stream(stream)), "mlp_tp_swiglu_forward")
+                                       _ptr(U), _ptr(Y), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mlp_tp_swiglu_forward")
 
 
 def mlp_tp_swiglu_backward(X, A, Wg, B, Ha, Hg, U, dY, T: int, h: int, f: int, t: int, dX, dA, dWg, dB,
@@ -220,9 +230,10 @@ def mlp_tp_swiglu_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
 
 
 def mlp_tp_attn_forward(X, Wqkv, Wo, b: int, s: int, h: int, a: int, d: int, t: int, causal: bool, QKV, C, L, Y,
-                        stream=None) -> None:
+                        workspace, workspace_bytes: int, stream=None) -> None:
     _check(lib().mlp_tp_attn_forward(_ptr(X), _ptr(Wqkv), _ptr(Wo), b, s, h, a, d, t, int(bool(causal)), _ptr(QKV),
-                                     _ptr(C), _ptr(L), _ptr(Y), _stream(stream)), "mlp_tp_attn_forward")
+                                     _ptr(C), _ptr(L), _ptr(Y), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mlp_tp_attn_forward")
 
 
 def mlp_tp_attn_workspace_bytes(b: int, s: int, h: int, a: int, d: int, t: int) -> int:

@@ -1,14 +1,27 @@
 """Device buffers and one-call helpers around the C ABI (allocation through PyTorch only).
 
 A user with their own buffers calls the C-ABI names in ``_lib`` directly; these helpers
-allocate the outputs and workspace on the current CUDA device and call the same entry
-points. No arithmetic of the block happens here.
+allocate the outputs and workspaces on the current CUDA device and call the same entry
+points. No arithmetic of the block happens here. The backward workspace ("ws") starts
+with the intermediates and ends with the split-tail region, whose last
+mlp_tp_forward_workspace_bytes() bytes the forward reuses as its optional workspace
+(the forward and backward of one buffer set run in stream order).
 """
 from __future__ import annotations
 
 import torch
 
-from ._lib import (mlp_tp_backward, mlp_tp_forward, mlp_tp_workspace_bytes)
+from ._lib import (mlp_tp_backward, mlp_tp_forward, mlp_tp_forward_workspace_bytes, mlp_tp_workspace_bytes)
+
+
+def _fwd_ws(buf: dict):
+    """The forward's optional workspace: the tail of the backward workspace."""
+    ws = buf["ws"]
+    n = mlp_tp_forward_workspace_bytes()
+    if ws.numel() < n:
+        return None, 0
+    off = (ws.numel() - n) // 256 * 256
+    return ws[off:], ws.numel() - off
 
 
 def empty_buffers(T: int, h: int, f: int, t: int, device="cuda") -> dict[str, torch.Tensor]:
@@ -33,8 +46,9 @@ def empty_buffers(T: int, h: int, f: int, t: int, device="cuda") -> dict[str, to
 def forward(inp: dict, buf: dict, t: int, stream=None) -> None:
     T, h = inp["X"].shape
     f = inp["A"].shape[1]
+    fws, fwn = _fwd_ws(buf)
     mlp_tp_forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], T, h, f, t,
-                   buf["H"], buf["G"], buf["Y"], stream)
+                   buf["H"], buf["G"], buf["Y"], fws, fwn, stream)
 
 
 def backward(inp: dict, buf: dict, t: int, stream=None) -> None:
@@ -70,8 +84,9 @@ def swiglu_forward(inp: dict, buf: dict, t: int, stream=None) -> None:
     from ._lib import mlp_tp_swiglu_forward
     T, h = inp["X"].shape
     f = inp["A"].shape[1]
+    fws, fwn = _fwd_ws(buf)
     mlp_tp_swiglu_forward(inp["X"], inp["A"], inp["Wg"], inp["B"], T, h, f, t, buf["Ha"], buf["Hg"], buf["U"],
-                          buf["Y"], stream)
+                          buf["Y"], fws, fwn, stream)
 
 
 def swiglu_backward(inp: dict, buf: dict, t: int, stream=None) -> None:
@@ -110,8 +125,9 @@ def attn_forward(inp: dict, buf: dict, b: int, s: int, a: int, t: int, causal: b
     from ._lib import mlp_tp_attn_forward
     h = inp["X"].shape[1]
     d = inp["Wqkv"].shape[1] // (3 * a)
+    fws, fwn = _fwd_ws(buf)
     mlp_tp_attn_forward(inp["X"], inp["Wqkv"], inp["Wo"], b, s, h, a, d, t, causal, buf["QKV"], buf["C"], buf["L"],
-                        buf["Y"], stream)
+                        buf["Y"], fws, fwn, stream)
 
 
 def attn_backward(inp: dict, buf: dict, b: int, s: int, a: int, t: int, causal: bool = True, stream=None) -> None:

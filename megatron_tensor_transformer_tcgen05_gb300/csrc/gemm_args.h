@@ -39,6 +39,12 @@ struct GemmArgs {
     // K concatenation: k blocks [0, kb_split) read (tmA, tmB), the rest read (tmA2, tmB2)
     // from their own k = 0, so D = A1 B1^T + A2 B2^T in one accumulator (0 = one segment).
     int kb_split;
+    // Split tail (EPI_PLAIN, EPI_BIAS only): the last split_tiles tiles of the tile order each
+    // run as split_k parts over consecutive ranges of k blocks; part p writes its fp32
+    // accumulator to split_ws[p * TM * OBN ...] and splitk_fixup_kernel sums them in order.
+    int split_tiles;             // 0 = every tile whole
+    int split_k;
+    float* split_ws;
     int* status;                 // device status word (first error code wins)
     DropoutParams drop;          // EPI_BIAS_DROPOUT_RES
     unsigned long long timeout_ns;
@@ -47,5 +53,11 @@ struct GemmArgs {
 // Defined in umma_gemm.cuh; explicitly instantiated once per flavour (gemm_*.cu).
 template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
+
+// After a GEMM launched with split_tiles > 0: out[m, n] = bf16(sum over the tile's parts in
+// order + bias[n]) for the split tiles (bias may be NULL). TM x BN is the GEMM's tile
+// (rows x output columns); out is row-major with leading dimension ld_out. One launch.
+cudaError_t launch_splitk_fixup(const GemmArgs& args, int TM, int BN, __nv_bfloat16* out, long long ld_out,
+                                cudaStream_t stream);
 
 }  // namespace mlp

@@ -5,4 +5,5 @@ namespace mlp {
 template cudaError_t launch_umma_gemm<128, false, false, EPI_PLAIN, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_PLAIN, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_PLAIN, 2>(const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_umma_gemm<512, false, false, EPI_PLAIN, 2>(const GemmArgs&, int, cudaStream_t);
 }  // namespace mlp

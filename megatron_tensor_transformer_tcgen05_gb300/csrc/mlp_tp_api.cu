@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -28,6 +29,22 @@ __device__ int g_device_status[kStatusWords];
 // Limit for every bounded wait inside the GEMMs: one wait never lasts longer than one
 // tile's main loop (well under a millisecond), so two seconds only trips on a real stall.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Kernel launches issued by the library since it was loaded (all devices and streams).
+static std::atomic<long long> g_launches{0};
+static void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Split tail workspace: room for one fp32 part per unit of up to 160 SMs (a part is a
+// 256 x 512 tile for a CTA pair, at most 128 x 256 for one CTA: 256 KB per SM).
+constexpr size_t kSplitWsBytes = size_t(160) * 256 * 1024;
+// CTA pairs take 512-wide tiles (25% fewer operand bytes per FLOP than 256-wide; one
+// accumulator, so each tile's epilogue delays the next tile's MMAs by about half an
+// epilogue) when N allows and the K loop is long enough to hide that delay.
+constexpr int kWideMinK = 2048;
+// Each part of a split tile runs at least this many 64-deep k blocks.
+constexpr int kMinSplitKb = 16;
+// The split region of a workspace: none when there are no tokens (no GEMM runs then).
+static size_t split_ws_bytes(long long tokens) { return tokens > 0 ? kSplitWsBytes : 0; }
 
 struct DeviceInfo {
     bool ready = false;
@@ -119,15 +136,47 @@ static bool map_store(CUtensorMap* m, const void* p, uint64_t cols, uint64_t row
 // Tile width along N: 256 when the N extent splits into whole 256-wide tiles, else 128.
 static int tile_n(int n) { return (n % 256 == 0) ? 256 : 128; }
 
-// CTA pairs (256-row tiles, cta_group::2) for 256-wide tiles over more than 128 rows.
-static bool use_pairs(int M, int BN) { return BN == 256 && M > 128; }
+// CTA pairs (256-row tiles, cta_group::2) for 256- and 512-wide tiles over more than 128 rows.
+static bool use_pairs(int M, int BN) { return BN >= 256 && M > 128; }
 
 // Rows of a K-major B operand one CTA loads per stage: half the tile width for a pair.
-static uint32_t kmajor_b_box(int M, int BN) { return use_pairs(M, BN) ? BN / 2 : BN; }
+static uint32_t kmajor_b_box(int M, int BN) { return use_pairs(M, BN) ? 128 : BN; }
+
+// Where a GEMM may put the parts of split tiles, and the output the fixup then writes
+// (row-major [M, N], the GEMM's only output).
+struct SplitOut {
+    float* ws = nullptr;
+    size_t ws_bytes = 0;
+    void* out = nullptr;
+};
+
+// The tiles % units tiles of the short last round (all tiles when there are fewer than
+// units) are cut into as many K ranges as keep the parts within one round of units, each
+// of at least kMinSplitKb k blocks, within the workspace; fewer than two parts: no split.
+static void choose_split(GemmArgs& g, long long tiles, int units, int TM, int BN, const SplitOut* so)
+{
+    g.split_tiles = 0;
+    g.split_k = 1;
+    g.split_ws = nullptr;
+    if (!so || !so->ws || !so->out || tiles <= 0 || units <= 1) return;
+    const long long rem = tiles % units;
+    if (rem == 0) return;
+    const int num_kb = (g.K + 63) / 64;
+    long long sk = units / rem;
+    sk = std::min<long long>(sk, num_kb / kMinSplitKb);
+    const size_t part_bytes = static_cast<size_t>(TM) * BN * 4;
+    sk = std::min<long long>(sk, static_cast<long long>(so->ws_bytes / (part_bytes * static_cast<size_t>(rem))));
+    if (sk < 2) return;
+    g.split_tiles = static_cast<int>(rem);
+    g.split_k = static_cast<int>(sk);
+    g.split_ws = so->ws;
+}
 
 template <bool A_MN, bool B_MN, int EPI>
-static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
+static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const SplitOut* so = nullptr)
 {
+    constexpr bool kSplittable = (EPI == EPI_PLAIN || EPI == EPI_BIAS);
+    if (!kSplittable) so = nullptr;
     // Keep the smaller operand resident in L2 and stream the larger one once: with A
     // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
     // B block; otherwise sweep N fastest so they share one A block.
@@ -136,18 +185,40 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s)
     // distinct operand blocks (DRAM traffic at 18B: 3.8-5.3 GB -> 2.5-2.9 GB per GEMM).
     const int units = use_pairs(g.M, BN) ? num_sms / 2 : num_sms;
     g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(units > 1 ? units : 1))));
+    if (use_pairs(g.M, BN) && g.N % 512 == 0 && g.K >= kWideMinK) BN = 512;
     const long long tiles_n = (g.N + BN - 1) / BN;
     if (use_pairs(g.M, BN)) {
-        // CTA pairs: 256 x 256 tiles, one pair per two SMs.
+        // CTA pairs: 256 x BN tiles, one pair per two SMs.
         const long long tiles = ((g.M + 255) / 256) * tiles_n;
-        const int pairs = static_cast<int>(tiles < num_sms / 2 ? tiles : num_sms / 2);
-        return launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s);
+        choose_split(g, tiles, num_sms / 2, 256, BN, so);
+        const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
+        const int pairs = static_cast<int>(work < num_sms / 2 ? work : num_sms / 2);
+        cudaError_t e = BN == 512 ? launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s)
+                                  : launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s);
+        if (e != cudaSuccess) return e;
+        note_launches(1);
+        if (g.split_tiles > 0) {
+            if ((e = launch_splitk_fixup(g, 256, BN, static_cast<__nv_bfloat16*>(so->out), g.N, s)) != cudaSuccess)
+                return e;
+            note_launches(1);
+        }
+        return cudaSuccess;
     }
     const long long tiles = ((g.M + 127) / 128) * tiles_n;
-    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    choose_split(g, tiles, num_sms, 128, BN, so);
+    const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
+    const int grid = static_cast<int>(work < num_sms ? work : num_sms);
     if (grid <= 0) return cudaSuccess;
-    return BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, grid, s)
-                     : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, grid, s);
+    cudaError_t e = BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, grid, s)
+                              : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, grid, s);
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    if (g.split_tiles > 0) {
+        if ((e = launch_splitk_fixup(g, 128, BN, static_cast<__nv_bfloat16*>(so->out), g.N, s)) != cudaSuccess)
+            return e;
+        note_launches(1);
+    }
+    return cudaSuccess;
 }
 
 // The SwiGLU up-projection: one 256-wide MMA per 128 output columns ([X A | X Wg]).
@@ -160,8 +231,10 @@ static cudaError_t gemm_dual(GemmArgs& g, int num_sms, cudaStream_t s)
     const long long tiles = static_cast<long long>((g.M + (pair ? 255 : 127)) / (pair ? 256 : 128)) * ((g.N + 127) / 128);
     const int grid_units = static_cast<int>(tiles < units ? tiles : units);
     if (grid_units <= 0) return cudaSuccess;
-    return pair ? launch_umma_gemm<256, false, true, EPI_SWIGLU, 2>(g, 2 * grid_units, s)
-                : launch_umma_gemm<256, false, true, EPI_SWIGLU, 1>(g, grid_units, s);
+    const cudaError_t e = pair ? launch_umma_gemm<256, false, true, EPI_SWIGLU, 2>(g, 2 * grid_units, s)
+                               : launch_umma_gemm<256, false, true, EPI_SWIGLU, 1>(g, grid_units, s);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -258,22 +331,25 @@ const char* mlp_tp_status_string(mlp_status s)
 }
 
 // Backward workspace: dH [T,f] bf16 | dH column sums per 32-row block [ceil(T/32), f] fp32 |
-// dY column sums per row slice [slices, h] fp32 (each region 256-byte aligned).
+// dY column sums per row slice [slices, h] fp32 | split-tail parts (kSplitWsBytes), each
+// region 256-byte aligned. The recompute backward puts G [T,f] bf16 right after dH.
 static size_t ws_dh_bytes(int T, int f) { return round256(static_cast<size_t>(T) * f * 2); }
 static size_t ws_rows_bytes(int T, int f) { return round256(static_cast<size_t>((T + 31) / 32) * f * 4); }
 static size_t ws_dy_bytes(int T, int h) { return round256(static_cast<size_t>(colsum_splits(T)) * h * 4); }
+static size_t bwd_ws_before_split(int T, int h, int f, bool recompute)
+{
+    return (recompute ? 2 : 1) * ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
+}
 
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t)
 {
     if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    return ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
+    return bwd_ws_before_split(T, h, f, false) + split_ws_bytes(T);
 }
 
-int mlp_tp_launches_per_call(int backward, int T)
-{
-    if (T <= 0) return 0;
-    return backward ? 6 : 2;
-}
+size_t mlp_tp_forward_workspace_bytes(void) { return kSplitWsBytes; }
+
+long long mlp_tp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
 
@@ -283,7 +359,8 @@ namespace mlp {
 // residual R, writing Z instead of Y.
 static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
                                const mlp_bf16* b, const mlp_bf16* R, const DropoutParams* drop, int T, int h,
-                               int f, int t, mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* cuda_stream)
+                               int f, int t, mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream)
 {
     mlp_status st = check_shape(T, h, f, t);
     if (st != MLP_OK) return st;
@@ -292,10 +369,12 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
     const void* ptrs[] = {X, A, a, B, b, H, G, Y, R};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != MLP_OK) return st;
     if (T == 0) return MLP_OK;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const SplitOut so{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, Y};
     const int fs = f / t;
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     CallTimer timer(s);
@@ -330,7 +409,7 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
         g2.drop = *drop;
         e = gemm<false, true, EPI_BIAS_DROPOUT_RES>(g2, bn_h, dev->num_sms, s);
     } else {
-        e = gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s);
+        e = gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s, &so);
     }
     if (e != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_DOWN);
@@ -355,9 +434,10 @@ extern "C" {
 
 mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
                           const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* G,
-                          mlp_bf16* Y, void* cuda_stream)
+                          mlp_bf16* Y, void* workspace, size_t workspace_bytes, void* cuda_stream)
 {
-    return forward_impl(X, A, a, B, b, nullptr, nullptr, T, h, f, t, H, G, Y, cuda_stream);
+    return forward_impl(X, A, a, B, b, nullptr, nullptr, T, h, f, t, H, G, Y, workspace, workspace_bytes,
+                        cuda_stream);
 }
 
 mlp_status mlp_tp_forward_residual_dropout(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
@@ -368,7 +448,7 @@ mlp_status mlp_tp_forward_residual_dropout(const mlp_bf16* X, const mlp_bf16* A,
 {
     DropoutParams d;
     if (!make_dropout(p, seed, offset, &d)) return MLP_EINVAL;
-    return forward_impl(X, A, a, B, b, R, &d, T, h, f, t, H, G, Z, cuda_stream);
+    return forward_impl(X, A, a, B, b, R, &d, T, h, f, t, H, G, Z, nullptr, 0, cuda_stream);
 }
 
 mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, unsigned long long seed,
@@ -392,6 +472,7 @@ mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, u
     dropout_backward_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(dZ), n8, d,
                                                                       reinterpret_cast<__nv_bfloat16*>(dY));
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_DROPOUT_BWD);
     return MLP_OK;
 }
@@ -435,6 +516,7 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
+    float* split_ws = reinterpret_cast<float*>(ws + bwd_ws_before_split(T, h, f, recompute));
     const size_t g_bytes = recompute ? ws_dh_bytes(T, f) : 0;  // the recomputed G follows dH
     mlp_bf16* Gw = recompute ? reinterpret_cast<mlp_bf16*>(ws + ws_dh_bytes(T, f)) : nullptr;
     float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + g_bytes);
@@ -471,7 +553,8 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g4.M = T; g4.N = h; g4.K = f;
     g4.status = dev->status;
     g4.timeout_ns = kWaitLimitNs;
-    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so4{split_ws, kSplitWsBytes, dX};
+    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s, &so4) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DX);
 
     // GEMM 5: dA = X^T*dH (M = h, N = f, K = T), both operands MN-major.
@@ -483,7 +566,8 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g5.M = h; g5.N = f; g5.K = T;
     g5.status = dev->status;
     g5.timeout_ns = kWaitLimitNs;
-    if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so5{split_ws, kSplitWsBytes, dA};
+    if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s, &so5) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DA);
 
     // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major.
@@ -495,7 +579,8 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g6.M = f; g6.N = h; g6.K = T;
     g6.status = dev->status;
     g6.timeout_ns = kWaitLimitNs;
-    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so6{split_ws, kSplitWsBytes, dB};
+    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s, &so6) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DB);
 
     // Bias gradients: db's partial column sums over row slices of dY (da's came out of the
@@ -504,10 +589,12 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     colsum_partial_kernel<<<dim3(strips_h, nsplit), kColsumThreads, 0, s>>>(
         nullptr, 0, reinterpret_cast<const __nv_bfloat16*>(dY), h, T, nsplit, dy_part);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_COLSUM_PARTIAL);
     bias_grad_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(dh_rows, (T + 31) / 32, f, dy_part, nsplit, h,
                                                                   da, db);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_COLSUM_FINAL);
     return MLP_OK;
 }
@@ -528,7 +615,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
 size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t)
 {
     if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    return 2 * ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
+    return bwd_ws_before_split(T, h, f, true) + split_ws_bytes(T);
 }
 
 mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
@@ -649,7 +736,9 @@ extern "C" mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, 
     if (st != MLP_OK) return st;
     if (limit_ns > 10000000000ull) return MLP_EINVAL;
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(cuda_stream)>>>(dev->status, limit_ns);
-    return cudaGetLastError() == cudaSuccess ? MLP_OK : MLP_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
+    return MLP_OK;
 }
 
 // ---- SwiGLU variant of the block ----------------------------------------------------------
@@ -657,12 +746,13 @@ extern "C" mlp_status mlp_tp_selftest_wait_timeout(unsigned long long limit_ns, 
 extern "C" size_t mlp_tp_swiglu_workspace_bytes(int T, int h, int f, int t)
 {
     if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    return 2 * round256(static_cast<size_t>(T) * f * 2);  // dHa, dHg
+    return 2 * round256(static_cast<size_t>(T) * f * 2) + split_ws_bytes(T);  // dHa, dHg, split-tail parts
 }
 
 extern "C" mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* Wg,
                                             const mlp_bf16* B, int T, int h, int f, int t, mlp_bf16* Ha,
-                                            mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* cuda_stream)
+                                            mlp_bf16* Hg, mlp_bf16* U, mlp_bf16* Y, void* workspace,
+                                            size_t workspace_bytes, void* cuda_stream)
 {
     mlp_status st = check_shape(T, h, f, t);
     if (st != MLP_OK) return st;
@@ -670,6 +760,7 @@ extern "C" mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A
     const void* ptrs[] = {X, A, Wg, B, Ha, Hg, U, Y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != MLP_OK) return st;
     if (T == 0) return MLP_OK;
@@ -694,7 +785,8 @@ extern "C" mlp_status mlp_tp_swiglu_forward(const mlp_bf16* X, const mlp_bf16* A
     g2.M = T; g2.N = h; g2.K = f;
     g2.status = dev->status;
     g2.timeout_ns = kWaitLimitNs;
-    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, Y};
+    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, s, &so) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_DOWN);
     return MLP_OK;
 }
@@ -728,6 +820,8 @@ extern "C" mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* 
     const int bn_f = tile_n(f / t), bn_h = tile_n(h);
     mlp_bf16* dHa = static_cast<mlp_bf16*>(workspace);
     mlp_bf16* dHg = reinterpret_cast<mlp_bf16*>(static_cast<uint8_t*>(workspace) + round256(static_cast<size_t>(T) * f * 2));
+    float* split_ws =
+        reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 2 * round256(static_cast<size_t>(T) * f * 2));
     CallTimer timer(s);
 
     // dU = dY B^T, and in the epilogue dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha).
@@ -756,7 +850,8 @@ extern "C" mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* 
     g4.kb_split = kb_f;
     g4.status = dev->status;
     g4.timeout_ns = kWaitLimitNs;
-    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so4{split_ws, kSplitWsBytes, dX};
+    if (gemm<false, false, EPI_PLAIN>(g4, bn_h, dev->num_sms, s, &so4) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DX);
 
     // dA = X^T dHa and dWg = X^T dHg.
@@ -769,7 +864,8 @@ extern "C" mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* 
         g5.M = h; g5.N = f; g5.K = T;
         g5.status = dev->status;
         g5.timeout_ns = kWaitLimitNs;
-        if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+        const SplitOut so5{split_ws, kSplitWsBytes, dWs[i]};
+        if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s, &so5) != cudaSuccess) return MLP_ECUDA;
         timer.mark(MLP_K_BWD_DA);
     }
 
@@ -780,7 +876,8 @@ extern "C" mlp_status mlp_tp_swiglu_backward(const mlp_bf16* X, const mlp_bf16* 
     g6.M = f; g6.N = h; g6.K = T;
     g6.status = dev->status;
     g6.timeout_ns = kWaitLimitNs;
-    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so6{split_ws, kSplitWsBytes, dB};
+    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s, &so6) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DB);
     return MLP_OK;
 }
@@ -848,6 +945,7 @@ extern "C" mlp_status mlp_tp_bias_grads_noalloc(const mlp_bf16* dH, const mlp_bf
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
     colsum_finalize_kernel<<<(f + h + 255) / 256, 256, 0, s>>>(partial, nsplit, f, h, da, db);
     if (cudaGetLastError() != cudaSuccess) return MLP_ECUDA;
+    note_launches(2);
     return MLP_OK;
 }
 
@@ -885,7 +983,8 @@ static size_t attn_ws_d(int b, int a, int s) { return round256(static_cast<size_
 
 extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo, int b, int s,
                                           int h, int a, int d, int t, int causal, mlp_bf16* QKV, mlp_bf16* Cctx,
-                                          float* L, mlp_bf16* Y, void* cuda_stream)
+                                          float* L, mlp_bf16* Y, void* workspace, size_t workspace_bytes,
+                                          void* cuda_stream)
 {
     mlp_status st = check_attn(b, s, h, a, d, t);
     if (st != MLP_OK) return st;
@@ -893,9 +992,12 @@ extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqk
     const void* ptrs[] = {X, Wqkv, Wo, QKV, Cctx, L, Y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != MLP_OK) return st;
     if (b == 0) return MLP_OK;
+    float* split_ws = static_cast<float*>(workspace);
+    const size_t split_bytes = workspace ? workspace_bytes : 0;
     cudaStream_t strm = static_cast<cudaStream_t>(cuda_stream);
     const int T = b * s, hd = a * d;
     CallTimer timer(strm);
@@ -908,7 +1010,8 @@ extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqk
     g1.M = T; g1.N = 3 * hd; g1.K = h;
     g1.status = dev->status;
     g1.timeout_ns = kWaitLimitNs;
-    if (gemm<false, true, EPI_PLAIN>(g1, tile_n(3 * hd), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so1{split_ws, split_bytes, QKV};
+    if (gemm<false, true, EPI_PLAIN>(g1, tile_n(3 * hd), dev->num_sms, strm, &so1) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_QKV);
 
     // Per head: scores, mask, softmax and P V on chip; C and L to HBM.
@@ -919,6 +1022,7 @@ extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqk
     at.out = reinterpret_cast<__nv_bfloat16*>(Cctx);
     at.lse = L;
     if (launch_attn_fwd(at, strm) != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_ATTN_FWD);
 
     // Y = C Wo: the sum over the t head shards is the K loop of one accumulator (K = a d).
@@ -928,7 +1032,8 @@ extern "C" mlp_status mlp_tp_attn_forward(const mlp_bf16* X, const mlp_bf16* Wqk
     g2.M = T; g2.N = h; g2.K = hd;
     g2.status = dev->status;
     g2.timeout_ns = kWaitLimitNs;
-    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so2{split_ws, split_bytes, Y};
+    if (gemm<false, true, EPI_PLAIN>(g2, tile_n(h), dev->num_sms, strm, &so2) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_OUT);
     return MLP_OK;
 }
@@ -937,7 +1042,7 @@ extern "C" size_t mlp_tp_attn_workspace_bytes(int b, int s, int h, int a, int d,
 {
     if (check_attn(b, s, h, a, d, t) != MLP_OK) return 0;
     const int T = b * s, hd = a * d;
-    return attn_ws_dc(T, hd) + attn_ws_d(b, a, s) + round256(static_cast<size_t>(T) * 3 * hd * 2);
+    return attn_ws_dc(T, hd) + attn_ws_d(b, a, s) + round256(static_cast<size_t>(T) * 3 * hd * 2) + split_ws_bytes(T);
 }
 
 extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* Wo,
@@ -969,6 +1074,8 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     mlp_bf16* dC = reinterpret_cast<mlp_bf16*>(ws);
     float* D = reinterpret_cast<float*>(ws + attn_ws_dc(T, hd));
     mlp_bf16* dQKV = reinterpret_cast<mlp_bf16*>(ws + attn_ws_dc(T, hd) + attn_ws_d(b, a, s));
+    float* split_ws = reinterpret_cast<float*>(ws + attn_ws_dc(T, hd) + attn_ws_d(b, a, s) +
+                                               round256(static_cast<size_t>(T) * 3 * hd * 2));
     CallTimer timer(strm);
 
     // dC = dY Wo^T (each head shard's rows of Wo).
@@ -980,7 +1087,8 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     g3.M = T; g3.N = hd; g3.K = h;
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
-    if (gemm<false, false, EPI_PLAIN>(g3, bn_hd, dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so3{split_ws, kSplitWsBytes, dC};
+    if (gemm<false, false, EPI_PLAIN>(g3, bn_hd, dev->num_sms, strm, &so3) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_DC);
 
     // dWo = C^T dY.
@@ -990,13 +1098,15 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     g4.M = hd; g4.N = h; g4.K = T;
     g4.status = dev->status;
     g4.timeout_ns = kWaitLimitNs;
-    if (gemm<true, true, EPI_PLAIN>(g4, tile_n(h), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so4{split_ws, kSplitWsBytes, dWo};
+    if (gemm<true, true, EPI_PLAIN>(g4, tile_n(h), dev->num_sms, strm, &so4) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_DWO);
 
     // D = rowsum(dC (.) C) per (token, head).
     if (launch_attn_bwd_dot(reinterpret_cast<const __nv_bfloat16*>(dC), reinterpret_cast<const __nv_bfloat16*>(Cctx),
                             T, s, a, D, dev->num_sms, strm) != cudaSuccess)
         return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_ATTN_DOT);
 
     // dQ: per 128-query block over 64-key blocks.
@@ -1009,6 +1119,7 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     aq.lse = const_cast<float*>(L);
     aq.delta = D;
     if (launch_attn_bwd_dq(aq, strm) != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_ATTN_DQ);
 
     // dK, dV: per 128-key block over 64-query blocks.
@@ -1018,6 +1129,7 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
         !make_map(&ak.tmdO, dC, hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return MLP_ECUDA;
     if (launch_attn_bwd_dkdv(ak, strm) != cudaSuccess) return MLP_ECUDA;
+    note_launches(1);
     timer.mark(MLP_K_ATTN_DKDV);
 
     // dX = dQKV Wqkv^T: one accumulator over K = 3 a d sums Q, K, V and all head shards.
@@ -1029,7 +1141,8 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     g6.M = T; g6.N = h; g6.K = 3 * hd;
     g6.status = dev->status;
     g6.timeout_ns = kWaitLimitNs;
-    if (gemm<false, false, EPI_PLAIN>(g6, bn_h, dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so6{split_ws, kSplitWsBytes, dX};
+    if (gemm<false, false, EPI_PLAIN>(g6, bn_h, dev->num_sms, strm, &so6) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_DX);
 
     // dWqkv = X^T dQKV.
@@ -1040,7 +1153,8 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     g7.M = h; g7.N = 3 * hd; g7.K = T;
     g7.status = dev->status;
     g7.timeout_ns = kWaitLimitNs;
-    if (gemm<true, true, EPI_PLAIN>(g7, tile_n(3 * hd), dev->num_sms, strm) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so7{split_ws, kSplitWsBytes, dWqkv};
+    if (gemm<true, true, EPI_PLAIN>(g7, tile_n(3 * hd), dev->num_sms, strm, &so7) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_ATTN_DWQKV);
     return MLP_OK;
 }

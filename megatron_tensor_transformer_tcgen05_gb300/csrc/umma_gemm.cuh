@@ -15,6 +15,12 @@
 //              swizzled staging in shared memory, TMA store of 32x32 boxes
 // The two accumulators let the epilogue of tile i overlap the main loop of tile i+1.
 //
+// Split tail (EPI_PLAIN and EPI_BIAS): when the tile count leaves the last round of tiles
+// short (tiles % units of them), those last tiles may each be cut into split_k ranges of
+// K, so the short round becomes up to one part per unit. A part writes its fp32 partial
+// accumulator to split_ws; splitk_fixup_kernel then adds the parts of each tile in order
+// (plus the bias) and writes the bf16 tile, so the result is the same on every run.
+//
 // Epilogues (the step of the MLP block each one implements):
 //   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H)            -> stores H and G
 //   EPI_BIAS       Y = acc + b[n]                          -> stores Y
@@ -44,7 +50,9 @@ template <int BN_, bool A_MN_, bool B_MN_, int EPI_, int CG_>
 struct GemmCfg {
     // CG = 1: one CTA computes a 128 x BN tile. CG = 2: a CTA pair (cluster of 2) computes a
     // 256 x BN tile with cta_group::2 MMAs; each CTA holds 128 rows of A, BN/2 rows of B and
-    // its 128 x BN half of the accumulator.
+    // its 128 x BN half of the accumulator. A 512-wide pair tile is two MMA halves of N = 256
+    // (CTA r holds B rows [256h + 128r, +128) of half h) into all 512 TMEM columns: one
+    // accumulator instead of two, for 25% fewer operand bytes per FLOP than 256 x 256.
     static constexpr int CG = CG_;
     static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int BN_CTA = BN / CG;  // rows of the B operand one CTA loads
@@ -54,24 +62,38 @@ struct GemmCfg {
     // its MMA N = BN spans [A's columns | Wg's columns] of that range.
     static constexpr bool DUAL = (EPI == EPI_SWIGLU);
     static constexpr int OBN = DUAL ? BN / 2 : BN;
+    static constexpr int HALVES = (BN == 512) ? 2 : 1;  // MMAs per k step, each N = MMA_N
+    static constexpr int MMA_N = BN / HALVES;
+    // accumulators in TMEM: two (the epilogue of tile i overlaps the main loop of tile i+1),
+    // or one 512-column accumulator whose halves are released one after the other
+    static constexpr int NACC = (BN == 512) ? 1 : 2;
+    // epilogues whose output is the accumulator (plus a bias): their last tiles may be split
+    static constexpr bool SPLITTABLE = (EPI == EPI_PLAIN || EPI == EPI_BIAS);
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NOUT =
         (EPI == EPI_SWIGLU) ? 3 : (EPI == EPI_BIAS_GELU || EPI == EPI_DSWIGLU || EPI == EPI_DGELU_G) ? 2 : 1;
     static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
-    static constexpr uint32_t EPI_BYTES = 4 * 2 * NOUT * STG_BYTES;  // 4 warps x 2 buffers
-    static constexpr uint32_t TMEM_COLS = 2 * BN;                    // two fp32 accumulators
+    // Epilogue warps: 8 (two per TMEM lane quadrant, taking alternate 32-column chunks) for the
+    // one-accumulator 512-wide tiles, whose epilogue holds up the next tile's MMAs until each
+    // half is read out; else 4. With 8, each warp stages through one buffer instead of two.
+    static constexpr int EPI_WARPS = (NACC == 1 && EPI != EPI_DGELU_G) ? 8 : 4;
+    static constexpr int EPI_SETS = EPI_WARPS / 4;
+    static constexpr int STG_BUFS = EPI_WARPS == 8 ? 1 : 2;
+    static constexpr uint32_t EPI_BYTES = EPI_WARPS * STG_BUFS * NOUT * STG_BYTES;
+    static constexpr uint32_t TMEM_COLS = NACC * BN;                 // fp32 accumulators
     // as many stages as fit beside the epilogue staging (at most 6 for pairs, 4 alone)
     static constexpr int STAGES_FIT = static_cast<int>((232448u - 1024u - 256u - EPI_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT < ((CG == 2) ? 6 : 4) ? STAGES_FIT : ((CG == 2) ? 6 : 4);
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
     static constexpr uint32_t BAR_BYTES = 8 * NUM_BARS + 16;
     static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    static constexpr int THREADS = 192;
-    static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, BN, A_MN, B_MN);
-    static_assert(BN == 128 || BN == 256, "tile width");
-    static_assert(CG == 1 || (CG == 2 && BN == 256), "CTA pairs use 256-wide tiles");
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA issuer, epilogue
+    static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, MMA_N, A_MN, B_MN);
+    static_assert(BN == 128 || BN == 256 || BN == 512, "tile width");
+    static_assert(CG == 1 ? BN <= 256 : (BN == 256 || (BN == 512 && !DUAL)), "CTA pairs use 256- or 512-wide tiles");
+    static_assert(TMEM_COLS <= 512, "tensor memory columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(STAGES >= 3, "pipeline depth");
     static_assert(!DUAL || (B_MN && BN == 256), "dual B operand: MN-major, 256-wide MMA");
@@ -214,8 +236,28 @@ __device__ __forceinline__ void tile_origin(int tile, int tiles_m, int tiles_n, 
     }
 }
 
+// Work unit u -> its tile, its range of k blocks [kb_lo, kb_hi) and, for a part of a split
+// tile, its index among all parts (part = -1 for a whole tile). Units [0, n_whole) are the
+// whole tiles in tile order; then each of the last split_tiles tiles comes as split_k parts.
+__device__ __forceinline__ void work_unit(int u, int n_whole, int split_k, int num_kb, int& tile, int& kb_lo,
+                                          int& kb_hi, int& part)
+{
+    if (u < n_whole) {
+        tile = u;
+        kb_lo = 0;
+        kb_hi = num_kb;
+        part = -1;
+        return;
+    }
+    const int v = u - n_whole, r = v / split_k, sk = v - r * split_k;
+    tile = n_whole + r;
+    part = v;
+    kb_lo = static_cast<int>(static_cast<long long>(sk) * num_kb / split_k);
+    kb_hi = static_cast<int>(static_cast<long long>(sk + 1) * num_kb / split_k);
+}
+
 template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
-__global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
+__global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
 {
     using C = GemmCfg<BN, A_MN, B_MN, EPI, CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -245,6 +287,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
     const int tiles_n = (N + C::OBN - 1) / C::OBN;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (K + C::BK - 1) / C::BK;
+    const int split_tiles = C::SPLITTABLE ? args.split_tiles : 0;
+    const int split_k = split_tiles > 0 ? args.split_k : 1;
+    const int n_whole = num_tiles - split_tiles;
+    const int num_work = n_whole + split_tiles * split_k;
     const unsigned long long limit = args.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -254,7 +300,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(b_accf + 8u * a, 1);
-            mbar_init(b_acce + 8u * a, 4 * CG);  // one arrive per epilogue warp of the pair
+            mbar_init(b_acce + 8u * a, C::EPI_WARPS * CG);  // one arrive per epilogue warp of the pair
         }
         mbar_init(b_drain, 1);
         *abort_flag = 0;
@@ -290,12 +336,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0, par = 0;
             bool ok = true;
-            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
+            for (int u = unit; ok && u < num_work; u += num_units) {
+                int tile, kb_lo, kb_hi, part;
+                work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
                 int m0, n0;
                 tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
                 const int m_cta = m0 + C::BM * static_cast<int>(rank);
                 const int n_cta = n0 + C::BN_CTA * static_cast<int>(rank);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(b_empty + 8u * stage, phase ^ 1u, abort_flag, args.status,
                                            limit, DEV_TIMEOUT_PRODUCER, tile, kb)) {
                         ok = false;
@@ -345,12 +393,19 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                             for (int i = 0; i < C::BN_CTA / 64; ++i)
                                 tma_load_2d_pair(sb + 8192u * i, rank == 0 ? &args.tmB : &args.tmB2, n0 + 64 * i,
                                                  k0, fb0);
-                        } else if (B_MN) {
+                        } else if (B_MN) {  // half h: 128 rows at sb + 16 KB h, in 64-wide boxes
 #pragma unroll
-                            for (int i = 0; i < C::BN_CTA / 64; ++i)
-                                tma_load_2d_pair(sb + 8192u * i, tB, n_cta + 64 * i, k0, fb0);
+                            for (int h = 0; h < C::HALVES; ++h)
+#pragma unroll
+                                for (int i = 0; i < 2; ++i)
+                                    tma_load_2d_pair(sb + 16384u * h + 8192u * i, tB,
+                                                     n0 + C::MMA_N * h + 128 * static_cast<int>(rank) + 64 * i, k0,
+                                                     fb0);
                         } else {
-                            tma_load_2d_pair(sb, tB, k0, n_cta, fb0);
+#pragma unroll
+                            for (int h = 0; h < C::HALVES; ++h)
+                                tma_load_2d_pair(sb + 16384u * h, tB, k0,
+                                                 n0 + C::MMA_N * h + 128 * static_cast<int>(rank), fb0);
                         }
                     }
                     issued |= 1u << stage;
@@ -379,7 +434,9 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
         if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true, any = false;
-            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
+            for (int u = unit; ok && u < num_work; u += num_units) {
+                int tile, kb_lo, kb_hi, part;
+                work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
                 if (!mbar_wait_bounded(b_acce + 8u * acc, acc_phase ^ 1u, abort_flag, args.status,
                                        limit, DEV_TIMEOUT_MMA_ACC, tile, -1)) {
                     ok = false;
@@ -387,7 +444,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                // one accumulator: half 1 may still be draining; its release is awaited just
+                // before the first MMA that writes it (after the first k block's half 0)
+                bool half1_free = C::NACC == 2;
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(b_full + 8u * stage, phase, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, tile, kb)) {
                         ok = false;
@@ -397,18 +457,33 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     const uint32_t sa = s_stages + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
-                        // K-major: next 16 elements are 32 bytes further along the swizzled row.
-                        // MN-major: next 16 k-rows are two 8-row (1024-byte) groups further.
-                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                                 : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                                 : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-                        if (CG == 2)
-                            umma_bf16_pair(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
-                        else
-                            umma_bf16(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                    for (int h = 0; h < C::HALVES; ++h) {
+                        if (h == 1 && !half1_free) {
+                            if (!mbar_wait_bounded(b_acce + 8u, acc_phase ^ 1u, abort_flag, args.status, limit,
+                                                   DEV_TIMEOUT_MMA_ACC, tile, -2)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            half1_free = true;
+                        }
+#pragma unroll
+                        for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
+                            // K-major: next 16 elements are 32 bytes further along the swizzled
+                            // row. MN-major: next 16 k-rows are two 8-row (1024-byte) groups on.
+                            const uint32_t sbh = sb + 16384u * h;
+                            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                                     : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+                            const uint64_t bd = B_MN ? smem_desc_sw128(sbh + 2048u * k, 8192u, 1024u)
+                                                     : smem_desc_sw128(sbh + 32u * k, 16u, 1024u);
+                            const uint32_t accum = (kb != kb_lo || k != 0) ? 1u : 0u;
+                            if (CG == 2)
+                                umma_bf16_pair(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
+                            else
+                                umma_bf16(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
+                        }
                     }
+                    if (!ok) break;
                     any = true;
                     // the stage is free, in both CTAs, once these MMAs finish
                     if (CG == 2)
@@ -426,8 +501,12 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     umma_commit_pair_both(b_accf + 8u * acc);
                 else
                     umma_commit(b_accf + 8u * acc);
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+                if (C::NACC == 2) {
+                    acc ^= 1u;
+                    if (acc == 0) acc_phase ^= 1u;
+                } else {
+                    acc_phase ^= 1u;
+                }
             }
             if (!ok && any) {
                 // Let the MMAs already issued finish before TMEM is released.
@@ -442,10 +521,13 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
     } else {
         // ------------------------------ epilogue ----------------------------------
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the ones this warp may read
+        const int ewarp = warp - 2, eset = ewarp >> 2;  // chunks eset, eset + EPI_SETS, ...
         // accumulator release goes to the even CTA, which issues the MMAs
         const uint32_t acce0 = (CG == 2) ? mapa_shared(b_acce, 0) : b_acce;
         uint32_t acc = 0, acc_phase = 0, sel = 0;
-        for (int tile = unit; tile < num_tiles; tile += num_units) {
+        for (int u = unit; u < num_work; u += num_units) {
+            int tile, kb_lo, kb_hi, part;
+            work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
             // One lane waits; the warp follows its verdict so the .sync.aligned TMEM loads
             // below always run with all 32 lanes.
             int ready = 0;
@@ -460,12 +542,18 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
             const int row_blk = m0 + C::BM * static_cast<int>(rank) + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+            // a part of a split tile: its fp32 accumulator, chunk c of 32 columns at
+            // [c][row within the tile][32] of this part's TM x OBN block of split_ws
+            float* part_out = nullptr;
+            if (C::SPLITTABLE && part >= 0)
+                part_out = args.split_ws + static_cast<size_t>(part) * TM * C::OBN +
+                           static_cast<size_t>(C::BM * static_cast<int>(rank) + 32 * q + lane) * 32;
 
             uint4 hnext[4], gnext[4];
             if (EPI == EPI_DGELU || EPI == EPI_DGELU_G || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int n = n0 + 8 * i;
+                    const int n = n0 + 32 * eset + 8 * i;
                     const bool in = row < M && n < N;
                     hnext[i] = in ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n) : make_uint4(0, 0, 0, 0);
                     if (EPI == EPI_DSWIGLU)
@@ -474,7 +562,7 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                 }
             }
 #pragma unroll 1
-            for (int c = 0; c < C::OBN / 32; ++c) {
+            for (int c = eset; c < C::OBN / 32; c += C::EPI_SETS) {
                 const int nc = n0 + 32 * c;
                 const bool active = nc < N;  // warp-uniform
                 uint32_t r[32], r2[32];
@@ -483,15 +571,31 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     if (C::DUAL) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(C::OBN) + 32u * c, r2);  // X Wg
                     tmem_ld_wait();
                 }
-                if (c == C::OBN / 32 - 1) {
+                // release: the whole accumulator after its last chunk, or (one 512-column
+                // accumulator) each 256-column half after its last chunk
+                const bool last_mine = c + C::EPI_SETS >= C::OBN / 32;
+                const bool release =
+                    C::NACC == 2 ? last_mine : (last_mine || (c < C::OBN / 64 && c + C::EPI_SETS >= C::OBN / 64));
+                if (release) {
+                    const uint32_t rel = C::NACC == 2 ? acc : (c >= C::OBN / 64 ? 1u : 0u);
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) {  // accumulator may be reused
+                    if (lane == 0) {  // accumulator (half) may be reused
                         if (CG == 2)
-                            mbar_arrive_cluster(acce0 + 8u * acc);
+                            mbar_arrive_cluster(acce0 + 8u * rel);
                         else
-                            mbar_arrive(b_acce + 8u * acc);
+                            mbar_arrive(b_acce + 8u * rel);
                     }
+                }
+                if (C::SPLITTABLE && part_out) {
+                    if (active) {
+                        float4* dst = reinterpret_cast<float4*>(part_out + static_cast<size_t>(c) * TM * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    }
+                    continue;
                 }
                 if (!active || row_blk >= M) continue;
 
@@ -514,10 +618,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                         unpack_bf16x8(hnext[i], ha + 8 * i);
                         unpack_bf16x8(gnext[i], hg + 8 * i);
                     }
-                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of Ha and Hg
+                    if (c + C::EPI_SETS < C::OBN / 32) {  // prefetch the next chunk of Ha and Hg
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int n = nc + 32 + 8 * i;
+                            const int n = nc + 32 * C::EPI_SETS + 8 * i;
                             const bool in = row < M && n < N;
                             const size_t o = static_cast<size_t>(row) * args.ld_aux + n;
                             hnext[i] = in ? ldg_nc_v4(args.aux + o) : make_uint4(0, 0, 0, 0);
@@ -547,10 +651,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     float rv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], rv + 8 * i);
-                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of the residual
+                    if (c + C::EPI_SETS < C::OBN / 32) {  // prefetch the next chunk of the residual
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int n = nc + 32 + 8 * i;
+                            const int n = nc + 32 * C::EPI_SETS + 8 * i;
                             hnext[i] = (row < M && n < N)
                                            ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
                                            : make_uint4(0, 0, 0, 0);
@@ -570,10 +674,10 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
-                    if (c + 1 < C::OBN / 32) {  // prefetch the next chunk of H
+                    if (c + C::EPI_SETS < C::OBN / 32) {  // prefetch the next chunk of H
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int n = nc + 32 + 8 * i;
+                            const int n = nc + 32 * C::EPI_SETS + 8 * i;
                             hnext[i] = (row < M && n < N)
                                            ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
                                            : make_uint4(0, 0, 0, 0);
@@ -606,8 +710,8 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                         p1[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]), gelu_tanh_f(v[2 * j + 1]));
                 }
 
-                const uint32_t buf0 = s_epi + ((q * 2 + sel) * C::NOUT) * C::STG_BYTES;
-                if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `sel` has read it
+                const uint32_t buf0 = s_epi + ((ewarp * C::STG_BUFS + sel) * C::NOUT) * C::STG_BYTES;
+                if (lane == 0) bulk_wait_group_read<C::STG_BUFS - 1>();  // the store that last used it has read it
                 __syncwarp();
                 stage_row_sw64(buf0, lane, p0);
                 if (C::NOUT >= 2) stage_row_sw64(buf0 + C::STG_BYTES, lane, p1);
@@ -620,10 +724,14 @@ __global__ void __launch_bounds__(192, 1) umma_gemm_kernel(const __grid_constant
                     if (C::NOUT >= 3) tma_store_2d(&args.tmD2, nc, row_blk, buf0 + 2 * C::STG_BYTES);
                     bulk_commit_group();
                 }
-                sel ^= 1u;
+                if (C::STG_BUFS == 2) sel ^= 1u;
             }
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            if (C::NACC == 2) {
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
         }
         if (lane == 0) bulk_wait_group<0>();
     }

@@ -157,6 +157,8 @@ def attn_flops(b: int, s: int, h: int, a: int, d: int, causal: bool) -> int:
 ATTN_WORKLOADS: dict[str, AttnWorkload] = {w.name: w for w in [
     AttnWorkload("attn-tiny", 2, 200, 256, 2, 2, sw=0.08, sdy=1.0,
                  desc="tiny head-parallel attention b=2 s=200 h=256 a=2 d=128 t=2, causal"),
+    AttnWorkload("attn-2k", 2, 2048, 2048, 16, 2,
+                 desc="small head-parallel attention b=2 s=2048 h=2048 a=16 d=128 t=2, causal"),
     AttnWorkload("gpt-18b-attn", 4, 2048, 6144, 48, 8,
                  desc="GPT 18B-shaped attention b=4 s=2048 h=6144 a=48 d=128 t=8, causal"),
     AttnWorkload("gpt3-175b-attn", 2, 2048, 12288, 96, 8,

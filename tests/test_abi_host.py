@@ -38,10 +38,21 @@ def test_workspace_bytes():
     assert _lib.mlp_tp_workspace_bytes(0, 64, 256, 2) > 0         # partials only
 
 
-def test_launch_counts():
-    assert _lib.mlp_tp_launches_per_call(False, 128) == 2
-    assert _lib.mlp_tp_launches_per_call(True, 128) == 6
-    assert _lib.mlp_tp_launches_per_call(True, 0) == 0
+def test_forward_workspace_bytes():
+    fw = _lib.mlp_tp_forward_workspace_bytes()
+    assert fw == 40 * 1024 * 1024  # one 256 KB part per SM of up to 160 SMs
+    # every backward workspace holds the split-tail region after its own intermediates
+    assert _lib.mlp_tp_workspace_bytes(128, 64, 256, 2) >= 128 * 256 * 2 + fw
+    assert _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 2) >= 2 * 128 * 256 * 2 + fw
+    assert _lib.mlp_tp_swiglu_workspace_bytes(128, 64, 256, 2) >= 2 * 128 * 256 * 2 + fw
+
+
+def test_rejected_calls_launch_nothing(L):
+    n0 = _lib.mlp_tp_launch_count()
+    assert n0 >= 0
+    L.mlp_tp_forward(*([FAKE] * 5), 128, 64, 256, 3, FAKE, FAKE, FAKE, None, 0, None)
+    L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, 2, 64, 256, 2, 64, 1, 1, FAKE, FAKE, FAKE, FAKE, None, 0, None)
+    assert _lib.mlp_tp_launch_count() == n0
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails its checks
@@ -56,13 +67,15 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails it
     (128, 0, 256, 2, "MLP_EINVAL"),
 ])
 def test_forward_rejects_bad_shapes(L, T, h, f, t, code):
-    st = L.mlp_tp_forward(*([FAKE] * 5), T, h, f, t, FAKE, FAKE, FAKE, None)
+    st = L.mlp_tp_forward(*([FAKE] * 5), T, h, f, t, FAKE, FAKE, FAKE, None, 0, None)
     assert st == _lib.STATUS_CODES[code]
 
 
 def test_forward_rejects_null_and_misaligned(L):
-    assert L.mlp_tp_forward(None, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None) == 1
-    assert L.mlp_tp_forward(FAKE + 8, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None) == 3
+    assert L.mlp_tp_forward(None, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert L.mlp_tp_forward(FAKE + 8, *([FAKE] * 4), 128, 64, 256, 2, FAKE, FAKE, FAKE, None, 0, None) == 3
+    # the optional split-tail workspace must be 256-byte aligned when given
+    assert L.mlp_tp_forward(*([FAKE] * 5), 128, 64, 256, 2, FAKE, FAKE, FAKE, FAKE + 16, 1 << 20, None) == 3
 
 
 def test_backward_rejects_bad_arguments(L):
@@ -77,7 +90,7 @@ def test_backward_rejects_bad_arguments(L):
 
 def test_binding_raises_named_error(L):
     with pytest.raises(_lib.MlpError) as ei:
-        _lib.mlp_tp_forward(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 64, 256, 3, FAKE, FAKE, FAKE, stream=0)
+        _lib.mlp_tp_forward(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 64, 256, 3, FAKE, FAKE, FAKE, None, 0, stream=0)
     assert ei.value.name == "MLP_ESHAPE"
 
 
@@ -102,7 +115,7 @@ def test_attention_workspace_and_shape_rules():
     (2, 64, 256, 2, 128, 0, "MLP_EINVAL"),
 ])
 def test_attention_rejects_bad_shapes(L, b, s, h, a, d, t, code):
-    st = L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, b, s, h, a, d, t, 1, FAKE, FAKE, FAKE, FAKE, None)
+    st = L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, b, s, h, a, d, t, 1, FAKE, FAKE, FAKE, FAKE, None, 0, None)
     assert st == _lib.STATUS_CODES[code]
     st = L.mlp_tp_attn_backward(*([FAKE] * 7), b, s, h, a, d, t, 1, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
     assert st == _lib.STATUS_CODES[code]
@@ -110,8 +123,9 @@ def test_attention_rejects_bad_shapes(L, b, s, h, a, d, t, code):
 
 def test_attention_rejects_null_misaligned_and_short_workspace(L):
     shp = (2, 64, 256, 2, 128, 1, 1)
-    assert L.mlp_tp_attn_forward(None, FAKE, FAKE, *shp, FAKE, FAKE, FAKE, FAKE, None) == 1
-    assert L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, *shp, FAKE + 8, FAKE, FAKE, FAKE, None) == 3
+    assert L.mlp_tp_attn_forward(None, FAKE, FAKE, *shp, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, *shp, FAKE + 8, FAKE, FAKE, FAKE, None, 0, None) == 3
+    assert L.mlp_tp_attn_forward(FAKE, FAKE, FAKE, *shp, FAKE, FAKE, FAKE, FAKE, FAKE + 16, 1 << 20, None) == 3
     ws = _lib.mlp_tp_attn_workspace_bytes(2, 64, 256, 2, 128, 1)
     args = [FAKE] * 7 + list(shp) + [FAKE] * 3
     assert L.mlp_tp_attn_backward(*args, FAKE, ws - 256, None) == _lib.STATUS_CODES["MLP_EWORKSPACE"]

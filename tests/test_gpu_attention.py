@@ -91,7 +91,7 @@ def test_no_tokens_zeroes_weight_gradients():
     buf = block.empty_attn_buffers(0, 8, h, a, D, 1)
     buf["dWqkv"].fill_(1.0)
     buf["dWo"].fill_(1.0)
-    _lib.mlp_tp_attn_forward(None, dev["Wqkv"], dev["Wo"], 0, 8, h, a, D, 1, True, None, None, None, None)
+    _lib.mlp_tp_attn_forward(None, dev["Wqkv"], dev["Wo"], 0, 8, h, a, D, 1, True, None, None, None, None, None, 0)
     _lib.mlp_tp_attn_backward(None, dev["Wqkv"], dev["Wo"], None, None, None, None, 0, 8, h, a, D, 1, True, None,
                               buf["dWqkv"], buf["dWo"], buf["ws"], buf["ws"].numel())
     assert not buf["dWqkv"].any() and not buf["dWo"].any()
@@ -107,7 +107,7 @@ def test_rejects_bad_arguments():
         args = dict(b=b, s=s, h=h, a=a, d=D, t=1, X=dev["X"], QKV=buf["QKV"])
         args.update(kw)
         _lib.mlp_tp_attn_forward(args["X"], dev["Wqkv"], dev["Wo"], args["b"], args["s"], args["h"], args["a"],
-                                 args["d"], args["t"], True, args["QKV"], buf["C"], buf["L"], buf["Y"])
+                                 args["d"], args["t"], True, args["QKV"], buf["C"], buf["L"], buf["Y"], None, 0)
 
     for kw, name in ((dict(d=64), "MLP_ESHAPE"), (dict(t=3), "MLP_ESHAPE"), (dict(h=250), "MLP_ESHAPE"),
                      (dict(s=0), "MLP_EINVAL"), (dict(X=None), "MLP_EINVAL"),

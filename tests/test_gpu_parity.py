@@ -117,11 +117,11 @@ def test_gpu_rejects_bad_arguments():
     buf = block.empty_buffers(128, 64, 256, 2)
     with pytest.raises(_lib.MlpError) as ei:
         _lib.mlp_tp_forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], 128, 64, 256, 3,
-                            buf["H"], buf["G"], buf["Y"])
+                            buf["H"], buf["G"], buf["Y"], None, 0)
     assert ei.value.name == "MLP_ESHAPE"
     with pytest.raises(_lib.MlpError) as ei:
         _lib.mlp_tp_forward(inp["X"].data_ptr() + 2, inp["A"], inp["a"], inp["B"], inp["b"], 128, 64,
-                            256, 2, buf["H"], buf["G"], buf["Y"])
+                            256, 2, buf["H"], buf["G"], buf["Y"], None, 0)
     assert ei.value.name == "MLP_EALIGN"
     with pytest.raises(_lib.MlpError) as ei:
         _lib.mlp_tp_backward(inp["X"], inp["A"], inp["B"], buf["H"], buf["G"], inp["dY"], 128, 64, 256, 2,
