@@ -82,6 +82,12 @@ struct GemmCfg {
     static constexpr int EPI_SETS = EPI_WARPS / 4;
     static constexpr int STG_BUFS = EPI_WARPS == 8 ? 1 : 2;
     static constexpr uint32_t EPI_BYTES = EPI_WARPS * STG_BUFS * NOUT * STG_BYTES;
+    // Epilogues whose first output is the accumulator (+ bias) rounded to bf16 read each
+    // half of a one-accumulator tile out of TMEM (packed, 16 words a chunk) and release it
+    // before staging and storing anything; the bias + GELU epilogue then computes G from
+    // the rounded H.
+    static constexpr bool DRAIN_FIRST =
+        NACC == 1 && EPI_WARPS == 8 && (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU);
     static constexpr uint32_t TMEM_COLS = NACC * BN;                 // fp32 accumulators
     // as many stages as fit beside the epilogue staging (at most 6 for pairs, 4 alone)
     static constexpr int STAGES_FIT = static_cast<int>((232448u - 1024u - 256u - EPI_BYTES) / STAGE_BYTES);
@@ -561,6 +567,75 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                                       : make_uint4(0, 0, 0, 0);
                 }
             }
+            if (C::DRAIN_FIRST && part_out == nullptr) {
+                constexpr int KPH = C::OBN / 64 / C::EPI_SETS;  // this warp's chunks per half
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pk[KPH][16];
+#pragma unroll
+                    for (int k = 0; k < KPH; ++k) {
+                        const int c = hh * (C::OBN / 64) + eset + k * C::EPI_SETS;
+                        const int nc = n0 + 32 * c;
+                        uint32_t r[32];
+                        if (nc < N) {  // warp-uniform
+                            tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                            tmem_ld_wait();
+                        }
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float bv[8];
+                                const int n = nc + 8 * i;
+                                const uint4 u = n < N ? ldg_nc_v4(args.bias + n) : make_uint4(0, 0, 0, 0);
+                                unpack_bf16x8(u, bv);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) v[8 * i + j] += bv[j];
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[k][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {  // this half of the accumulator may be reused
+                        if (CG == 2)
+                            mbar_arrive_cluster(acce0 + 8u * hh);
+                        else
+                            mbar_arrive(b_acce + 8u * hh);
+                    }
+#pragma unroll
+                    for (int k = 0; k < KPH; ++k) {
+                        const int c = hh * (C::OBN / 64) + eset + k * C::EPI_SETS;
+                        const int nc = n0 + 32 * c;
+                        if (nc >= N || row_blk >= M) continue;
+                        uint32_t p1[16];
+                        if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float h0 = __uint_as_float(pk[k][j] << 16);
+                                const float h1 = __uint_as_float(pk[k][j] & 0xFFFF0000u);
+                                p1[j] = pack_bf16x2(gelu_tanh_f(h0), gelu_tanh_f(h1));
+                            }
+                        }
+                        const uint32_t buf0 = s_epi + ((ewarp * C::STG_BUFS + sel) * C::NOUT) * C::STG_BYTES;
+                        if (lane == 0) bulk_wait_group_read<C::STG_BUFS - 1>();  // its last store has read it
+                        __syncwarp();
+                        stage_row_sw64(buf0, lane, pk[k]);
+                        if (C::NOUT >= 2) stage_row_sw64(buf0 + C::STG_BYTES, lane, p1);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&args.tmD0, nc, row_blk, buf0);
+                            if (C::NOUT >= 2) tma_store_2d(&args.tmD1, nc, row_blk, buf0 + C::STG_BYTES);
+                            bulk_commit_group();
+                        }
+                        if (C::STG_BUFS == 2) sel ^= 1u;
+                    }
+                }
+            } else
 #pragma unroll 1
             for (int c = eset; c < C::OBN / 32; c += C::EPI_SETS) {
                 const int nc = n0 + 32 * c;
