@@ -39,8 +39,9 @@ static void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_rel
 constexpr size_t kSplitWsBytes = size_t(160) * 256 * 1024;
 // CTA pairs take 512-wide tiles (25% fewer operand bytes per FLOP than 256-wide; one
 // accumulator, so each tile's epilogue delays the next tile's MMAs by about half an
-// epilogue) when N allows and the K loop is long enough to hide that delay.
-constexpr int kWideMinK = 2048;
+// epilogue) when N allows and the K loop is long enough to hide that delay: K >= 2048 for
+// the epilogues that only round the accumulator (+ bias), K >= 4096 for those with math.
+constexpr int kWideMinK = 2048, kWideMinKMath = 4096;
 // Each part of a split tile runs at least this many 64-deep k blocks.
 constexpr int kMinSplitKb = 16;
 // The split region of a workspace: none when there are no tokens (no GEMM runs then).
@@ -185,7 +186,8 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     // distinct operand blocks (DRAM traffic at 18B: 3.8-5.3 GB -> 2.5-2.9 GB per GEMM).
     const int units = use_pairs(g.M, BN) ? num_sms / 2 : num_sms;
     g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(units > 1 ? units : 1))));
-    if (use_pairs(g.M, BN) && g.N % 512 == 0 && g.K >= kWideMinK) BN = 512;
+    const int wide_min_k = (EPI == EPI_PLAIN || EPI == EPI_BIAS) ? kWideMinK : kWideMinKMath;
+    if (use_pairs(g.M, BN) && g.N % 512 == 0 && g.K >= wide_min_k) BN = 512;
     const long long tiles_n = (g.N + BN - 1) / BN;
     if (use_pairs(g.M, BN)) {
         // CTA pairs: 256 x BN tiles, one pair per two SMs.

@@ -38,7 +38,8 @@ def _splits(M: int, N: int, K: int, BN: int) -> int:
     round of parts, within the forward workspace."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = BN == 256 and M > 128
-    if pairs and N % 512 == 0 and K >= 2048:  # CTA pairs then take 512-wide tiles
+    if pairs and N % 512 == 0 and K >= 2048:  # CTA pairs then take 512-wide tiles (the plain and
+        # bias epilogues of every GEMM checked here; those with math need K >= 4096)
         BN = 512
     TM, units = (256, sms // 2) if pairs else (128, sms)
     tiles = -(-M // TM) * -(-N // BN)
