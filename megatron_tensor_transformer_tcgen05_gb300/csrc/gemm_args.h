@@ -43,6 +43,9 @@ struct GemmArgs {
     // run as split_k parts over consecutive ranges of k blocks; part p writes its fp32
     // accumulator to split_ws[p * TM * OBN ...] and splitk_fixup_kernel sums them in order.
     int split_tiles;             // 0 = every tile whole
+    // CTA pairs per cluster for 512-wide pair tiles: 2 = a work tile is 512 x 512, the two
+    // pairs' rows, and each stage's B is fetched once and multicast to both pairs; else 1.
+    int cluster_pairs;
     int split_k;
     float* split_ws;
     int* status;                 // device status word (first error code wins)
@@ -53,6 +56,10 @@ struct GemmArgs {
 // Defined in umma_gemm.cuh; explicitly instantiated once per flavour (gemm_*.cu).
 template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
+
+// Clusters of `cluster` CTAs of that flavour that can be resident at once (0 on error).
+template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
+int umma_gemm_max_clusters(int cluster, int num_sms);
 
 // After a GEMM launched with split_tiles > 0: out[m, n] = bf16(sum over the tile's parts in
 // order + bias[n]) for the split tiles (bias may be NULL). TM x BN is the GEMM's tile

@@ -7,8 +7,10 @@ template cudaError_t launch_umma_gemm<128, false, false, EPI_DGELU, 1>(const Gem
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU, 2>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<512, false, false, EPI_DGELU, 2>(const GemmArgs&, int, cudaStream_t);
+template int umma_gemm_max_clusters<512, false, false, EPI_DGELU, 2>(int, int);
 template cudaError_t launch_umma_gemm<128, false, false, EPI_DGELU_G, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU_G, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DGELU_G, 2>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<512, false, false, EPI_DGELU_G, 2>(const GemmArgs&, int, cudaStream_t);
+template int umma_gemm_max_clusters<512, false, false, EPI_DGELU_G, 2>(int, int);
 }  // namespace mlp

@@ -6,4 +6,5 @@ template cudaError_t launch_umma_gemm<128, false, false, EPI_PLAIN, 1>(const Gem
 template cudaError_t launch_umma_gemm<256, false, false, EPI_PLAIN, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_PLAIN, 2>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<512, false, false, EPI_PLAIN, 2>(const GemmArgs&, int, cudaStream_t);
+template int umma_gemm_max_clusters<512, false, false, EPI_PLAIN, 2>(int, int);
 }  // namespace mlp

@@ -4,10 +4,10 @@
 namespace mlp {
 
 // Block (r, c): split tile r, output columns [32c, 32c + 32) of it; thread = row of the
-// tile. Each thread reads its row's 32 fp32 values from each part (128 contiguous bytes;
-// consecutive rows are consecutive), adds the parts in index order, then the bias, and
-// writes 32 bf16 with round-to-nearest-even.
-__global__ void __launch_bounds__(256) splitk_fixup_kernel(const float* __restrict__ ws, int split_k, int n_whole,
+// tile (up to 512 rows: a cluster's two CTA pairs). Each thread reads its row's 32 fp32
+// values from each part (128 contiguous bytes; consecutive rows are consecutive), adds the
+// parts in index order, then the bias, and writes 32 bf16 with round-to-nearest-even.
+__global__ void __launch_bounds__(512) splitk_fixup_kernel(const float* __restrict__ ws, int split_k, int n_whole,
                                                            int tiles_m, int tiles_n, int n_fastest, int group,
                                                            int TM, int BN, int M, int N,
                                                            const __nv_bfloat16* __restrict__ bias,

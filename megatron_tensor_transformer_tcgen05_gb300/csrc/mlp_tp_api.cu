@@ -42,6 +42,26 @@ constexpr size_t kSplitWsBytes = size_t(160) * 256 * 1024;
 // epilogue) when N allows and the K loop is long enough to hide that delay: K >= 2048 for
 // the epilogues that only round the accumulator (+ bias), K >= 4096 for those with math.
 constexpr int kWideMinK = 2048, kWideMinKMath = 4096;
+// 512-wide pair tiles run two pairs per cluster (512 x 512 work tiles, each stage's B fetched
+// once and multicast to both pairs) when the rows make whole 512-row tiles and clusters of
+// four cover at least 90% of the SMs. On a GB300 36 clusters fit (144 of 152 SMs): the
+// multicast saves enough operand traffic that the power-capped clock rises ~5%, more than
+// the idle SMs cost (175b step -2.7%, same-session A/B).
+constexpr bool kClusterPairs = true;
+
+// Clusters of four CTAs of this 512-wide flavour that fit at once, looked up once per SM count.
+template <bool A_MN, bool B_MN, int EPI>
+static int quad_clusters(int num_sms)
+{
+    static std::mutex mu;
+    static int for_sms = -1, clusters = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (for_sms != num_sms) {
+        clusters = umma_gemm_max_clusters<512, A_MN, B_MN, EPI, 2>(4, num_sms);
+        for_sms = num_sms;
+    }
+    return clusters;
+}
 // Each part of a split tile runs at least this many 64-deep k blocks.
 constexpr int kMinSplitKb = 16;
 // The split region of a workspace: none when there are no tokens (no GEMM runs then).
@@ -189,6 +209,29 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     const int wide_min_k = (EPI == EPI_PLAIN || EPI == EPI_BIAS) ? kWideMinK : kWideMinKMath;
     if (use_pairs(g.M, BN) && g.N % 512 == 0 && g.K >= wide_min_k) BN = 512;
     const long long tiles_n = (g.N + BN - 1) / BN;
+    g.cluster_pairs = 1;
+    if (kClusterPairs && BN == 512 && ((g.M + 255) / 256) % 2 == 0) {
+        const int quads = std::min(quad_clusters<A_MN, B_MN, EPI>(num_sms), num_sms / 4);
+        if (quads > 0 && 4 * quads * 10 >= 9 * num_sms) {
+            // two CTA pairs per cluster: 512 x 512 work tiles, one cluster per four SMs
+            g.cluster_pairs = 2;
+            g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(quads))));
+            const long long tiles = ((g.M + 511) / 512) * tiles_n;
+            choose_split(g, tiles, quads, 512, 512, so);
+            const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
+            const int clusters = static_cast<int>(work < quads ? work : quads);
+            cudaError_t e = launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, 4 * clusters, s);
+            if (e != cudaSuccess) return e;
+            note_launches(1);
+            if (g.split_tiles > 0) {
+                if ((e = launch_splitk_fixup(g, 512, 512, static_cast<__nv_bfloat16*>(so->out), g.N, s)) !=
+                    cudaSuccess)
+                    return e;
+                note_launches(1);
+            }
+            return cudaSuccess;
+        }
+    }
     if (use_pairs(g.M, BN)) {
         // CTA pairs: 256 x BN tiles, one pair per two SMs.
         const long long tiles = ((g.M + 255) / 256) * tiles_n;

@@ -1,6 +1,7 @@
 // sm103_ptx.cuh -- hand-written inline-PTX wrappers for sm_103a: mbarrier with bounded
 // waits, TMA tile copies (cp.async.bulk.tensor), and the tcgen05 tensor-core / TMEM ops.
-// No multicast of any kind is used. Every wait here is bounded: it gives up after a time
+// The one multicast is a TMA load within this GPU's memory to two CTAs of one cluster
+// (tma_load_2d_pair_mc); commits are unicast. Every wait here is bounded: it gives up after a time
 // limit, records an error code in a device status word and returns false, so a kernel
 // never spins forever.
 #pragma once
@@ -183,6 +184,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// As tma_load_2d_pair, multicast: the box lands at the same shared-memory offset in every CTA
+// of `cta_mask` (cluster ranks), and each destination's bytes complete on the barrier at
+// `bar_cluster`'s offset in the even CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                                    uint32_t bar_cluster, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
+        : "memory");
+}
+
 // shared -> global, 2-D tile; rows/columns beyond the tensor's extent are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int x, int y, uint32_t src)
 {
@@ -305,11 +319,12 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar)
 }
 
 // Pair form: arrive on the barrier at offset `bar` in both CTAs of the pair (two unicast
-// commits: this CTA's own barrier, then the peer's through its mapa address).
-__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar)
+// commits: this CTA's own barrier, then the peer's, cluster rank `peer`, through its mapa
+// address).
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar, uint32_t peer = 1u)
 {
     umma_commit_pair(bar);
-    umma_commit_pair(mapa_shared(bar, 1u));
+    umma_commit_pair(mapa_shared(bar, peer));
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.

@@ -8,7 +8,8 @@
 // row-major tensor); the tcgen05 instruction descriptor carries the major-ness, so no
 // operand is ever transposed in memory.
 //
-// Roles in one CTA (192 threads, one CTA per SM, persistent over output tiles):
+// Roles in one CTA (one CTA per SM, persistent over output tiles; 192 threads, or 320 with
+// eight epilogue warps):
 //   warp 0     TMA producer: fills a 4-stage ring of {A 128x64, B BNx64} tiles (128B swizzle)
 //   warp 1     allocates TMEM (two BN-column fp32 accumulators) and issues tcgen05.mma
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused element-wise math, bf16 RNE,
@@ -282,13 +283,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (s_slot + 4u - base));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Pair mode: rank 0 (the even CTA) issues every MMA; rank r owns rows [128r, 128r+128)
-    // of each 256-row tile and B rows [r*BN/2, (r+1)*BN/2) of each stage.
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int unit = (CG == 2) ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-    const int num_units = (CG == 2) ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+    // Pair mode: rank 0 (the even CTA) of a pair issues every MMA; rank r owns rows
+    // [128r, 128r+128) of each 256-row tile and B rows [r*BN/2, (r+1)*BN/2) of each stage.
+    // With two pairs per cluster (512-wide tiles only), pair p computes rows [256p, 256p+256)
+    // of a 512-row work tile, and the pairs share each stage's B: CTA (p, r) fetches B half p
+    // and multicasts it to CTA r of both pairs.
+    const int npc = (CG == 2 && C::HALVES == 2 && args.cluster_pairs == 2) ? 2 : 1;  // pairs per cluster
+    const uint32_t crank = (CG == 2) ? cluster_ctarank() : 0u;
+    const uint32_t rank = crank & 1u, pidx = crank >> 1, lead = crank & ~1u;
+    const int unit = static_cast<int>(blockIdx.x) / (CG * npc);
+    const int num_units = static_cast<int>(gridDim.x) / (CG * npc);
     const int M = args.M, N = args.N, K = args.K;
-    const int TM = C::BM * CG;  // rows per tile
+    const int TM = C::BM * CG * npc;  // rows per work tile
+    const int prow = C::BM * CG * static_cast<int>(pidx);  // this pair's first row in it
     const int tiles_m = (M + TM - 1) / TM;
     const int tiles_n = (N + C::OBN - 1) / C::OBN;
     const int num_tiles = tiles_m * tiles_n;
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(b_full + 8u * s, 1);
-            mbar_init(b_empty + 8u * s, 1);
+            mbar_init(b_empty + 8u * s, npc);  // each pair's MMAs release the stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(b_accf + 8u * a, 1);
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
                 int m0, n0;
                 tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
-                const int m_cta = m0 + C::BM * static_cast<int>(rank);
+                const int m_cta = m0 + prow + C::BM * static_cast<int>(rank);
                 const int n_cta = n0 + C::BN_CTA * static_cast<int>(rank);
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(b_empty + 8u * stage, phase ^ 1u, abort_flag, args.status,
@@ -386,7 +393,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     } else {
                         // Both CTAs' bytes complete on the even CTA's barrier, which the even
                         // CTA alone arms with the pair's total.
-                        const uint32_t fb0 = mapa_shared(fb, 0);
+                        const uint32_t fb0 = mapa_shared(fb, lead);
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
                         if (A_MN) {
                             tma_load_2d_pair(sa, tA, m_cta, k0, fb0);
@@ -399,6 +406,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                             for (int i = 0; i < C::BN_CTA / 64; ++i)
                                 tma_load_2d_pair(sb + 8192u * i, rank == 0 ? &args.tmB : &args.tmB2, n0 + 64 * i,
                                                  k0, fb0);
+                        } else if (npc == 2) {  // B half `pidx` to CTA `rank` of both pairs
+                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+                            const int nb = n0 + C::MMA_N * static_cast<int>(pidx) + 128 * static_cast<int>(rank);
+                            const uint32_t sbh = sb + 16384u * pidx;
+                            if (B_MN) {
+                                tma_load_2d_pair_mc(sbh, tB, nb, k0, fb0, mask);
+                                tma_load_2d_pair_mc(sbh + 8192u, tB, nb + 64, k0, fb0, mask);
+                            } else {
+                                tma_load_2d_pair_mc(sbh, tB, k0, nb, fb0, mask);
+                            }
                         } else if (B_MN) {  // half h: 128 rows at sb + 16 KB h, in 64-wide boxes
 #pragma unroll
                             for (int h = 0; h < C::HALVES; ++h)
@@ -491,11 +508,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     }
                     if (!ok) break;
                     any = true;
-                    // the stage is free, in both CTAs, once these MMAs finish
-                    if (CG == 2)
-                        umma_commit_pair_both(b_empty + 8u * stage);
-                    else
+                    // the stage is free, in both CTAs (and, with two pairs, in the other pair's,
+                    // which multicast into it), once these MMAs finish
+                    if (CG == 2) {
+                        umma_commit_pair_both(b_empty + 8u * stage, lead + 1u);
+                        if (npc == 2) {
+                            const uint32_t other = lead ^ 2u;
+                            umma_commit_pair(mapa_shared(b_empty + 8u * stage, other));
+                            umma_commit_pair(mapa_shared(b_empty + 8u * stage, other + 1u));
+                        }
+                    } else {
                         umma_commit(b_empty + 8u * stage);
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -504,7 +528,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 if (!ok) break;
                 // accumulator ready for the epilogue warps of both CTAs
                 if (CG == 2)
-                    umma_commit_pair_both(b_accf + 8u * acc);
+                    umma_commit_pair_both(b_accf + 8u * acc, lead + 1u);
                 else
                     umma_commit(b_accf + 8u * acc);
                 if (C::NACC == 2) {
@@ -529,7 +553,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the ones this warp may read
         const int ewarp = warp - 2, eset = ewarp >> 2;  // chunks eset, eset + EPI_SETS, ...
         // accumulator release goes to the even CTA, which issues the MMAs
-        const uint32_t acce0 = (CG == 2) ? mapa_shared(b_acce, 0) : b_acce;
+        const uint32_t acce0 = (CG == 2) ? mapa_shared(b_acce, lead) : b_acce;
         uint32_t acc = 0, acc_phase = 0, sel = 0;
         for (int u = unit; u < num_work; u += num_units) {
             int tile, kb_lo, kb_hi, part;
@@ -545,7 +569,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             tc_fence_after();
             int m0, n0;
             tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
-            const int row_blk = m0 + C::BM * static_cast<int>(rank) + 32 * q;
+            const int row_blk = m0 + prow + C::BM * static_cast<int>(rank) + 32 * q;
             const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
             // a part of a split tile: its fp32 accumulator, chunk c of 32 columns at
@@ -553,7 +577,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             float* part_out = nullptr;
             if (C::SPLITTABLE && part >= 0)
                 part_out = args.split_ws + static_cast<size_t>(part) * TM * C::OBN +
-                           static_cast<size_t>(C::BM * static_cast<int>(rank) + 32 * q + lane) * 32;
+                           static_cast<size_t>(prow + C::BM * static_cast<int>(rank) + 32 * q + lane) * 32;
 
             uint4 hnext[4], gnext[4];
             if (EPI == EPI_DGELU || EPI == EPI_DGELU_G || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
@@ -842,7 +866,7 @@ cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = (CG == 2 && C::HALVES == 2 && args.cluster_pairs == 2) ? 4 : CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -850,6 +874,33 @@ cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream
     e = cudaLaunchKernelEx(&cfg, kern, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
+int umma_gemm_max_clusters(int cluster, int num_sms)
+{
+    using C = GemmCfg<BN, A_MN, B_MN, EPI, CG>;
+    auto kern = umma_gemm_kernel<BN, A_MN, B_MN, EPI, CG>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES)) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms / cluster * cluster), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace mlp

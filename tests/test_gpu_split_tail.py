@@ -32,16 +32,7 @@ def _tile_n(n: int) -> int:
     return 256 if n % 256 == 0 else 128
 
 
-def _splits(M: int, N: int, K: int, BN: int) -> int:
-    """1 when the library's split rule (include/mlp_tp.h, "Split tails") cuts this GEMM's
-    last round, else 0: rounds of `units` tiles, parts of >= 16 k blocks of 64, at most one
-    round of parts, within the forward workspace."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    pairs = BN == 256 and M > 128
-    if pairs and N % 512 == 0 and K >= 2048:  # CTA pairs then take 512-wide tiles (the plain and
-        # bias epilogues of every GEMM checked here; those with math need K >= 4096)
-        BN = 512
-    TM, units = (256, sms // 2) if pairs else (128, sms)
+def _split_rule(TM: int, BN: int, units: int, M: int, N: int, K: int) -> int:
     tiles = -(-M // TM) * -(-N // BN)
     rem = tiles % units
     if rem == 0:
@@ -50,18 +41,42 @@ def _splits(M: int, N: int, K: int, BN: int) -> int:
     return 1 if sk >= 2 else 0
 
 
+def _splits(M: int, N: int, K: int, BN: int) -> set:
+    """The fixup launches (0 or 1) the library's split rule (include/mlp_tp.h, "Split tails")
+    can give this GEMM: rounds of `units` tiles, parts of >= 16 k blocks of 64, at most one
+    round of parts, within the forward workspace. Two answers where the tile shape depends
+    on how many clusters of four CTAs the device can hold."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = BN == 256 and M > 128
+    if pairs and N % 512 == 0 and K >= 2048:  # CTA pairs then take 512-wide tiles (the plain and
+        # bias epilogues of every GEMM checked here; those with math need K >= 4096)
+        BN = 512
+    TM, units = (256, sms // 2) if pairs else (128, sms)
+    out = {_split_rule(TM, BN, units, M, N, K)}
+    if BN == 512 and -(-M // 256) % 2 == 0:  # or two pairs per cluster, 512-row tiles
+        out.add(_split_rule(512, 512, sms // 4, M, N, K))
+    return out
+
+
+def _sums(*sets) -> set:
+    out = {0}
+    for s in sets:
+        out = {a + b for a in out for b in s}
+    return out
+
+
 def _mlp_fixups(T, h, f, t):
-    fwd = _splits(T, h, f, _tile_n(h))                                   # Y = G B + b
-    bwd = (_splits(T, h, f, _tile_n(h)) + _splits(h, f, T, _tile_n(f // t)) +  # dX, dA
-           _splits(f, h, T, _tile_n(h)))                                 # dB
+    fwd = _splits(T, h, f, _tile_n(h))                                         # Y = G B + b
+    bwd = _sums(_splits(T, h, f, _tile_n(h)), _splits(h, f, T, _tile_n(f // t)),  # dX, dA
+                _splits(f, h, T, _tile_n(h)))                                  # dB
     return fwd, bwd
 
 
 def _attn_fixups(b, s, h, a):
     T, hd = b * s, a * D
-    fwd = _splits(T, 3 * hd, h, _tile_n(3 * hd)) + _splits(T, h, hd, _tile_n(h))      # QKV, Y
-    bwd = (_splits(T, hd, h, _tile_n(hd)) + _splits(hd, h, T, _tile_n(h)) +            # dC, dWo
-           _splits(T, h, 3 * hd, _tile_n(h)) + _splits(h, 3 * hd, T, _tile_n(3 * hd)))  # dX, dWqkv
+    fwd = _sums(_splits(T, 3 * hd, h, _tile_n(3 * hd)), _splits(T, h, hd, _tile_n(h)))     # QKV, Y
+    bwd = _sums(_splits(T, hd, h, _tile_n(hd)), _splits(hd, h, T, _tile_n(h)),             # dC, dWo
+                _splits(T, h, 3 * hd, _tile_n(h)), _splits(h, 3 * hd, T, _tile_n(3 * hd)))  # dX, dWqkv
     return fwd, bwd
 
 
@@ -76,7 +91,7 @@ def _counted(fn):
 @pytest.mark.parametrize("T,h,f,t", [(128, 1024, 8192, 4), (512, 1024, 4096, 2), (2048, 256, 1024, 2)])
 def test_mlp_split_tails_match_oracle(T, h, f, t):
     fx_fwd, fx_bwd = _mlp_fixups(T, h, f, t)
-    if fx_fwd + fx_bwd == 0:
+    if max(fx_fwd) + max(fx_bwd) == 0:
         pytest.skip("no GEMM of this shape splits on this device's SM count")
     inp = make_inputs(T, h, f, seed=T + h, sdy=1.0)
     dev = {k: v.cuda() for k, v in inp.items()}
@@ -84,7 +99,8 @@ def test_mlp_split_tails_match_oracle(T, h, f, t):
     n_fwd = _counted(lambda: block.forward(dev, buf, t))
     n_bwd = _counted(lambda: block.backward(dev, buf, t))
     assert _lib.mlp_tp_query_device_status() == 0, _lib.mlp_tp_last_device_where()
-    assert (n_fwd, n_bwd) == (2 + fx_fwd, 6 + fx_bwd)
+    assert n_fwd - 2 in fx_fwd and n_bwd - 6 in fx_bwd, (n_fwd, n_bwd, fx_fwd, fx_bwd)
+    assert n_fwd + n_bwd > 8  # at least one split tail ran
     ref = oracle.fwd_bwd(inp)
     for k in ("H", "G", "Y", "dX", "dA", "dB", "da", "db"):
         assert_close(k, buf[k], ref[k])
@@ -103,7 +119,7 @@ def test_mlp_split_tails_match_oracle(T, h, f, t):
 def test_attention_split_tails_match_oracle():
     b, s, h, a, t = 1, 1024, 2048, 16, 2
     fx_fwd, fx_bwd = _attn_fixups(b, s, h, a)
-    if fx_fwd + fx_bwd == 0:
+    if max(fx_fwd) + max(fx_bwd) == 0:
         pytest.skip("no GEMM of this shape splits on this device's SM count")
     inp = make_attn_inputs(b, s, h, a, D, seed=11, sw=1.2 / np.sqrt(h), sdy=1.0)
     dev = {k: v.cuda() for k, v in inp.items()}
@@ -111,7 +127,8 @@ def test_attention_split_tails_match_oracle():
     n_fwd = _counted(lambda: block.attn_forward(dev, buf, b, s, a, t, True))
     n_bwd = _counted(lambda: block.attn_backward(dev, buf, b, s, a, t, True))
     assert _lib.mlp_tp_query_device_status() == 0, _lib.mlp_tp_last_device_where()
-    assert (n_fwd, n_bwd) == (3 + fx_fwd, 7 + fx_bwd)
+    assert n_fwd - 3 in fx_fwd and n_bwd - 7 in fx_bwd, (n_fwd, n_bwd, fx_fwd, fx_bwd)
+    assert n_fwd + n_bwd > 10  # at least one split tail ran
     ref = oracle.attn_fwd_bwd({k: v.double().numpy() for k, v in inp.items() if k != "Wqkv"}, b, s, a, True)
     # bf16 roundings on each path, as in the attention parity tests
     for name, n, got, want in (("QKV", 1, buf["QKV"], np.concatenate([ref["Q"], ref["K"], ref["V"]], axis=1)),
