@@ -75,7 +75,8 @@ typedef enum {
 
 typedef uint16_t mlp_bf16;
 
-/* Forward pass: H = X*A + a and G = GELU(H) (first GEMM, bias and GELU in its epilogue),
+/* Forward pass: H = X*A + a and G = GELU(H) (first GEMM, bias and GELU in its epilogue; G is
+ * computed from H as stored, rounded to bf16),
  * then Y = G*B + b (second GEMM; its K loop runs over the t shards' row blocks of B into
  * one accumulator, so the shard sum never leaves the chip). H and G are the activations
  * the backward needs ("Distributed training", section 2.2: the MLP keeps the GELU input
@@ -187,11 +188,11 @@ size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
  * backward of the block when the forward's G was not kept: the caller may pass the forward
  * any scratch buffer for G (one shared by every layer) and keep only H. The dH GEMM's
  * epilogue recomputes G = GELU(H) from the stored bf16 H (from the sigmoid GELU' needs
- * anyway) into the workspace, and dB = G^T dY reads it there. dX, dA, da and db are bitwise
- * those of mlp_tp_backward; dB differs only by G being recomputed from the rounded H.
- * Workspace (256-byte aligned, at least mlp_tp_recompute_workspace_bytes): dH [T,f] bf16 |
- * G [T,f] bf16 | the reduction partials | split-tail parts; dH and G are there on return. Other arguments and
- * errors as mlp_tp_backward. */
+ * anyway) into the workspace, and dB = G^T dY reads it there. The forward computes G from
+ * the rounded H too, so the recomputed G and every gradient are bitwise those of
+ * mlp_tp_backward. Workspace (256-byte aligned, at least mlp_tp_recompute_workspace_bytes):
+ * dH [T,f] bf16 | G [T,f] bf16 | the reduction partials | split-tail parts; dH and G are
+ * there on return. Other arguments and errors as mlp_tp_backward. */
 size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t);
 mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
                                      const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX, mlp_bf16* dA,

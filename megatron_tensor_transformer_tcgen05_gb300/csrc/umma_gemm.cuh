@@ -23,7 +23,8 @@
 // (plus the bias) and writes the bf16 tile, so the result is the same on every run.
 //
 // Epilogues (the step of the MLP block each one implements):
-//   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H)            -> stores H and G
+//   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H) of H rounded to bf16 (so a backward that
+//                  recomputes G from the stored H gets the same bits)  -> stores H and G
 //   EPI_BIAS       Y = acc + b[n]                          -> stores Y
 //   EPI_BIAS_DROPOUT_RES  Z = R[m,n] + keep(m,n) (acc + b[n]) / (1 - p)   -> stores Z
 //                  (keep from Philox4x32-10 on the element's index; philox.cuh)
@@ -803,10 +804,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                if (EPI == EPI_BIAS_GELU) {
+                if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H, as in every path
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p1[j] = pack_bf16x2(gelu_tanh_f(v[2 * j]), gelu_tanh_f(v[2 * j + 1]));
+                        p1[j] = pack_bf16x2(gelu_tanh_f(__uint_as_float(p0[j] << 16)),
+                                            gelu_tanh_f(__uint_as_float(p0[j] & 0xFFFF0000u)));
                 }
 
                 const uint32_t buf0 = s_epi + ((ewarp * C::STG_BUFS + sel) * C::NOUT) * C::STG_BYTES;

@@ -29,6 +29,7 @@ def test_backward_with_gelu_recompute(T, h, f, t):
     block.forward(dev, buf, t)
     block.backward(dev, buf, t)  # the reference: the backward that reads the forward's G
     kept = {k: buf[k].clone() for k in ("dX", "dA", "dB", "da", "db")}
+    G_fwd = buf["G"].clone()
     buf["G"].fill_(float("nan"))  # the forward's G was scratch: the recompute must not read it
     ws_bytes = _lib.mlp_tp_recompute_workspace_bytes(T, h, f, t)
     ws = torch.empty((ws_bytes,), dtype=torch.uint8, device="cuda")
@@ -38,9 +39,13 @@ def test_backward_with_gelu_recompute(T, h, f, t):
     assert _lib.mlp_tp_query_device_status() == 0
     for k in ("dX", "dA", "da", "db"):  # these never touch G: bitwise the kept-G backward
         assert torch.equal(out[k], kept[k]), k
+    # the forward computes G from the rounded H, as the recompute must: the same G to the bit,
+    # hence the same dB
+    G_rec = ws[((T * f * 2 + 255) // 256) * 256:][: T * f * 2].view(torch.bfloat16).view(T, f)
+    assert torch.equal(G_rec, G_fwd)
+    assert torch.equal(out["dB"], kept["dB"])
     ref = oracle.fwd_bwd({k: v.double().numpy() for k, v in inp.items()})
     assert_close("dB", out["dB"], ref["dB"])
-    G_rec = ws[((T * f * 2 + 255) // 256) * 256:][: T * f * 2].view(torch.bfloat16).view(T, f)
     assert_close("G recomputed", G_rec, ref["G"])
     fs = f // t
     for i in range(t):
