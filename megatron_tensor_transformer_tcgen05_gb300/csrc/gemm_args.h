@@ -39,7 +39,7 @@ struct GemmArgs {
     // K concatenation: k blocks [0, kb_split) read (tmA, tmB), the rest read (tmA2, tmB2)
     // from their own k = 0, so D = A1 B1^T + A2 B2^T in one accumulator (0 = one segment).
     int kb_split;
-    // Split tail (EPI_PLAIN, EPI_BIAS only): the last split_tiles tiles of the tile order each
+    // Split tail (EPI_PLAIN, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU): the last split_tiles tiles of the tile order each
     // run as split_k parts over consecutive ranges of k blocks; part p writes its fp32
     // accumulator to split_ws[p * TM * OBN ...] and splitk_fixup_kernel sums them in order.
     int split_tiles;             // 0 = every tile whole
@@ -61,10 +61,11 @@ cudaError_t launch_umma_gemm(const GemmArgs& args, int grid, cudaStream_t stream
 template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 int umma_gemm_max_clusters(int cluster, int num_sms);
 
-// After a GEMM launched with split_tiles > 0: out[m, n] = bf16(sum over the tile's parts in
-// order + bias[n]) for the split tiles (bias may be NULL). TM x BN is the GEMM's tile
-// (rows x output columns); out is row-major with leading dimension ld_out. One launch.
-cudaError_t launch_splitk_fixup(const GemmArgs& args, int TM, int BN, __nv_bfloat16* out, long long ld_out,
-                                cudaStream_t stream);
+// After a GEMM launched with split_tiles > 0: for the split tiles, the sum of each tile's
+// parts in order, then the epilogue `epi` (EPI_PLAIN, EPI_BIAS, EPI_BIAS_GELU: out0 = H,
+// out1 = G; EPI_DGELU: out0 = dH, and args.colsum_rows when set). TM x BN is the GEMM's work
+// tile (rows x output columns); outputs are row-major with leading dimension ld_out. One launch.
+cudaError_t launch_splitk_fixup(const GemmArgs& args, int epi, int TM, int BN, __nv_bfloat16* out0,
+                                __nv_bfloat16* out1, long long ld_out, cudaStream_t stream);
 
 }  // namespace mlp

@@ -169,6 +169,7 @@ struct SplitOut {
     float* ws = nullptr;
     size_t ws_bytes = 0;
     void* out = nullptr;
+    void* out1 = nullptr;  // G of the bias + GELU epilogue
 };
 
 // The tiles % units tiles of the short last round (all tiles when there are fewer than
@@ -196,7 +197,7 @@ static void choose_split(GemmArgs& g, long long tiles, int units, int TM, int BN
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const SplitOut* so = nullptr)
 {
-    constexpr bool kSplittable = (EPI == EPI_PLAIN || EPI == EPI_BIAS);
+    constexpr bool kSplittable = (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU);
     if (!kSplittable) so = nullptr;
     // Keep the smaller operand resident in L2 and stream the larger one once: with A
     // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
@@ -224,7 +225,7 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
             if (e != cudaSuccess) return e;
             note_launches(1);
             if (g.split_tiles > 0) {
-                if ((e = launch_splitk_fixup(g, 512, 512, static_cast<__nv_bfloat16*>(so->out), g.N, s)) !=
+                if ((e = launch_splitk_fixup(g, EPI, 512, 512, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) !=
                     cudaSuccess)
                     return e;
                 note_launches(1);
@@ -243,7 +244,7 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
         if (e != cudaSuccess) return e;
         note_launches(1);
         if (g.split_tiles > 0) {
-            if ((e = launch_splitk_fixup(g, 256, BN, static_cast<__nv_bfloat16*>(so->out), g.N, s)) != cudaSuccess)
+            if ((e = launch_splitk_fixup(g, EPI, 256, BN, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) != cudaSuccess)
                 return e;
             note_launches(1);
         }
@@ -259,7 +260,7 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     if (e != cudaSuccess) return e;
     note_launches(1);
     if (g.split_tiles > 0) {
-        if ((e = launch_splitk_fixup(g, 128, BN, static_cast<__nv_bfloat16*>(so->out), g.N, s)) != cudaSuccess)
+        if ((e = launch_splitk_fixup(g, EPI, 128, BN, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) != cudaSuccess)
             return e;
         note_launches(1);
     }
@@ -419,7 +420,7 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
     if ((st = device_info(&dev)) != MLP_OK) return st;
     if (T == 0) return MLP_OK;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const SplitOut so{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, Y};
+    const SplitOut so{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, Y, nullptr};
     const int fs = f / t;
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     CallTimer timer(s);
@@ -433,7 +434,8 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
     g1.bias = reinterpret_cast<const __nv_bfloat16*>(a);
     g1.status = dev->status;
     g1.timeout_ns = kWaitLimitNs;
-    if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s) != cudaSuccess) return MLP_ECUDA;
+    const SplitOut so1{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, H, G};
+    if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s, &so1) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_UP);
 
     // GEMM 2: Y = sum over shards of G_i*B_i, + b (then dropout and + R). One accumulator
@@ -584,8 +586,9 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g3.colsum_rows = dh_rows;  // da's per-32-row partial sums come out of this epilogue
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
+    const SplitOut so3{split_ws, kSplitWsBytes, dH, nullptr};
     const cudaError_t e3 = recompute ? gemm<false, false, EPI_DGELU_G>(g3, bn_f, dev->num_sms, s)
-                                     : gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s);
+                                     : gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s, &so3);
     if (e3 != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DH);
 

@@ -16,11 +16,11 @@
 //              swizzled staging in shared memory, TMA store of 32x32 boxes
 // The two accumulators let the epilogue of tile i overlap the main loop of tile i+1.
 //
-// Split tail (EPI_PLAIN and EPI_BIAS): when the tile count leaves the last round of tiles
-// short (tiles % units of them), those last tiles may each be cut into split_k ranges of
-// K, so the short round becomes up to one part per unit. A part writes its fp32 partial
-// accumulator to split_ws; splitk_fixup_kernel then adds the parts of each tile in order
-// (plus the bias) and writes the bf16 tile, so the result is the same on every run.
+// Split tail (EPI_PLAIN, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU): when the tile count leaves the
+// last round of tiles short (tiles % units of them), those last tiles may each be cut into
+// split_k ranges of K, so the short round becomes up to one part per unit. A part writes its
+// fp32 partial accumulator to split_ws; splitk_fixup_kernel then adds the parts of each tile
+// in order and applies the epilogue, so the result is the same on every run.
 //
 // Epilogues (the step of the MLP block each one implements):
 //   EPI_BIAS_GELU  H = acc + a[n]; G = GELU(H) of H rounded to bf16 (so a backward that
@@ -69,8 +69,9 @@ struct GemmCfg {
     // accumulators in TMEM: two (the epilogue of tile i overlaps the main loop of tile i+1),
     // or one 512-column accumulator whose halves are released one after the other
     static constexpr int NACC = (BN == 512) ? 1 : 2;
-    // epilogues whose output is the accumulator (plus a bias): their last tiles may be split
-    static constexpr bool SPLITTABLE = (EPI == EPI_PLAIN || EPI == EPI_BIAS);
+    // epilogues the split-tail fixup can finish: their last tiles may be split
+    static constexpr bool SPLITTABLE =
+        (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU);
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;

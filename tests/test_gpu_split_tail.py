@@ -41,16 +41,15 @@ def _split_rule(TM: int, BN: int, units: int, M: int, N: int, K: int) -> int:
     return 1 if sk >= 2 else 0
 
 
-def _splits(M: int, N: int, K: int, BN: int) -> set:
+def _splits(M: int, N: int, K: int, BN: int, math: bool = False) -> set:
     """The fixup launches (0 or 1) the library's split rule (include/mlp_tp.h, "Split tails")
     can give this GEMM: rounds of `units` tiles, parts of >= 16 k blocks of 64, at most one
     round of parts, within the forward workspace. Two answers where the tile shape depends
     on how many clusters of four CTAs the device can hold."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = BN == 256 and M > 128
-    if pairs and N % 512 == 0 and K >= 2048:  # CTA pairs then take 512-wide tiles (the plain and
-        # bias epilogues of every GEMM checked here; those with math need K >= 4096)
-        BN = 512
+    if pairs and N % 512 == 0 and K >= (4096 if math else 2048):  # CTA pairs then take 512-wide
+        BN = 512  # tiles (epilogues with math, bias + GELU and GELU', need the longer K)
     TM, units = (256, sms // 2) if pairs else (128, sms)
     out = {_split_rule(TM, BN, units, M, N, K)}
     if BN == 512 and -(-M // 256) % 2 == 0:  # or two pairs per cluster, 512-row tiles
@@ -66,8 +65,9 @@ def _sums(*sets) -> set:
 
 
 def _mlp_fixups(T, h, f, t):
-    fwd = _splits(T, h, f, _tile_n(h))                                         # Y = G B + b
-    bwd = _sums(_splits(T, h, f, _tile_n(h)), _splits(h, f, T, _tile_n(f // t)),  # dX, dA
+    up = _splits(T, f, h, _tile_n(f // t), math=True)                          # H, G; and dH
+    fwd = _sums(up, _splits(T, h, f, _tile_n(h)))                              # Y = G B + b
+    bwd = _sums(up, _splits(T, h, f, _tile_n(h)), _splits(h, f, T, _tile_n(f // t)),  # dX, dA
                 _splits(f, h, T, _tile_n(h)))                                  # dB
     return fwd, bwd
 
@@ -86,9 +86,11 @@ def _counted(fn):
     return _lib.mlp_tp_launch_count() - n0
 
 
-# (T, h, f, t): one CTA per tile (T = 128) splitting Y and dX; CTA pairs splitting Y and
-# dX; CTA pairs splitting dA and dB (K = T)
-@pytest.mark.parametrize("T,h,f,t", [(128, 1024, 8192, 4), (512, 1024, 4096, 2), (2048, 256, 1024, 2)])
+# (T, h, f, t): one CTA per tile (T = 128) splitting Y and dX; clusters of two pairs splitting
+# Y and dX; CTA pairs splitting dA and dB (K = T); 256-wide pairs splitting the bias + GELU
+# (H, G) and GELU' (dH and its column sums for da) GEMMs; clusters of two pairs splitting those
+@pytest.mark.parametrize("T,h,f,t", [(128, 1024, 8192, 4), (512, 1024, 4096, 2), (2048, 256, 1024, 2),
+                                     (512, 2048, 2048, 2), (512, 4096, 2048, 2)])
 def test_mlp_split_tails_match_oracle(T, h, f, t):
     fx_fwd, fx_bwd = _mlp_fixups(T, h, f, t)
     if max(fx_fwd) + max(fx_bwd) == 0:
