@@ -8,13 +8,21 @@
 // row-major tensor); the tcgen05 instruction descriptor carries the major-ness, so no
 // operand is ever transposed in memory.
 //
-// Roles in one CTA (one CTA per SM, persistent over output tiles; 192 threads, or 320 with
+// Roles in one CTA (one CTA per SM, persistent over work tiles; 192 threads, or 320 with
 // eight epilogue warps):
-//   warp 0     TMA producer: fills a 4-stage ring of {A 128x64, B BNx64} tiles (128B swizzle)
-//   warp 1     allocates TMEM (two BN-column fp32 accumulators) and issues tcgen05.mma
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused element-wise math, bf16 RNE,
-//              swizzled staging in shared memory, TMA store of 32x32 boxes
-// The two accumulators let the epilogue of tile i overlap the main loop of tile i+1.
+//   warp 0     TMA producer: fills a ring of {A 128 x 64, B (its share) x 64} stages (128B
+//              swizzle)
+//   warp 1     allocates TMEM and issues tcgen05.mma (in a CTA pair, the even CTA's alone)
+//   warps 2-5 (2-9)  epilogue: tcgen05.ld of the accumulator, fused element-wise math, bf16
+//              RNE, swizzled staging in shared memory, TMA store of 32x32 boxes
+// Tile shapes (GemmCfg): one CTA, 128 x BN (BN = 128, 256), two accumulators; a CTA pair
+// (cta_group::2), 256 x 256, two accumulators; a CTA pair, 256 x 512, one accumulator of all
+// 512 TMEM columns, released in two halves. With two accumulators the epilogue of tile i
+// overlaps the main loop of tile i+1; with one, the next tile's first MMAs wait for half 0 to
+// be read out, and its first half-1 MMA for half 1. A 512-wide pair tile may also run as one
+// of the two pairs of a cluster of four (args.cluster_pairs = 2): the pairs compute the two
+// 256-row halves of a 512 x 512 work tile, and CTA (p, r) fetches only B half p of each
+// stage and multicasts it to CTA r of both pairs.
 //
 // Split tail (EPI_PLAIN, EPI_BIAS, EPI_BIAS_GELU, EPI_DGELU): when the tile count leaves the
 // last round of tiles short (tiles % units of them), those last tiles may each be cut into
@@ -393,8 +401,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                             tma_load_2d(sb, tB, k0, n_cta, fb);
                         }
                     } else {
-                        // Both CTAs' bytes complete on the even CTA's barrier, which the even
-                        // CTA alone arms with the pair's total.
+                        // Both CTAs' bytes complete on the pair's even CTA's barrier, which that
+                        // CTA alone arms with the pair's total (with two pairs, the B half the
+                        // other pair multicasts into this pair completes there too).
                         const uint32_t fb0 = mapa_shared(fb, lead);
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
                         if (A_MN) {
