@@ -930,27 +930,50 @@ __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const __nv_bfloat16* 
                                                           const __nv_bfloat16* __restrict__ Cc, int T, int s, int a,
                                                           float* __restrict__ D)
 {
-    const int lane = threadIdx.x & 31;
-    const long long total = static_cast<long long>(T) * a;
+    // Rows are (token, head) pairs of 128 contiguous elements, consecutive in memory. A warp
+    // takes 4 consecutive rows per step (1 KB of each tensor, fully coalesced): 8 lanes per
+    // row, 16 elements (two 16-byte loads of each tensor) per lane, then a 3-step shuffle sum.
+    // Two steps in flight per warp keep enough bytes outstanding to run at HBM speed.
+    const int lane = threadIdx.x & 31, sub = lane & 7;
+    const long long rows = static_cast<long long>(T) * a;
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
-        const long long t = w / a;
-        const int head = static_cast<int>(w % a);
-        const size_t off = static_cast<size_t>(t) * a * kHeadDim + static_cast<size_t>(head) * kHeadDim + 4 * lane;
-        const uint2 u = *reinterpret_cast<const uint2*>(dC + off);
-        const uint2 v = *reinterpret_cast<const uint2*>(Cc + off);
-        const uint32_t uu[2] = {u.x, u.y}, vv[2] = {v.x, v.y};
-        float acc = 0.0f;
+    const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    for (long long g = 4 * w0; g < rows; g += 8 * nwarps) {
+        float acc[2] = {0.0f, 0.0f};
+        uint4 u[2][2], v[2][2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            acc = fmaf(__uint_as_float(uu[i] << 16), __uint_as_float(vv[i] << 16), acc);
-            acc = fmaf(__uint_as_float(uu[i] & 0xFFFF0000u), __uint_as_float(vv[i] & 0xFFFF0000u), acc);
+        for (int k = 0; k < 2; ++k) {
+            const long long w = g + 4 * nwarps * k + (lane >> 3);
+            if (w < rows) {
+                const size_t off = static_cast<size_t>(w) * kHeadDim + 16 * sub;
+                u[k][0] = __ldg(reinterpret_cast<const uint4*>(dC + off));
+                u[k][1] = __ldg(reinterpret_cast<const uint4*>(dC + off + 8));
+                v[k][0] = __ldg(reinterpret_cast<const uint4*>(Cc + off));
+                v[k][1] = __ldg(reinterpret_cast<const uint4*>(Cc + off + 8));
+            } else {
+                u[k][0] = u[k][1] = v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) {
-            const long long bi = t / s, p = t % s;
-            D[(bi * a + head) * s + p] = acc;
+        for (int k = 0; k < 2; ++k) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t uu[4] = {u[k][h].x, u[k][h].y, u[k][h].z, u[k][h].w};
+                const uint32_t vv[4] = {v[k][h].x, v[k][h].y, v[k][h].z, v[k][h].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[k] = fmaf(__uint_as_float(uu[i] << 16), __uint_as_float(vv[i] << 16), acc[k]);
+                    acc[k] = fmaf(__uint_as_float(uu[i] & 0xFFFF0000u), __uint_as_float(vv[i] & 0xFFFF0000u), acc[k]);
+                }
+            }
+#pragma unroll
+            for (int o = 4; o >= 1; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+            const long long w = g + 4 * nwarps * k + (lane >> 3);
+            if (sub == 0 && w < rows) {
+                const long long t = w / a, bi = t / s, p = t % s;
+                const int head = static_cast<int>(w % a);
+                D[(bi * a + head) * s + p] = acc[k];
+            }
         }
     }
 }
@@ -992,9 +1015,9 @@ cudaError_t launch_attn_bwd_dkdv(const AttnArgs& args, cudaStream_t stream)
 cudaError_t launch_attn_bwd_dot(const __nv_bfloat16* dC, const __nv_bfloat16* Cc, int T, int s, int a, float* D,
                                 int num_sms, cudaStream_t stream)
 {
-    const long long warps = static_cast<long long>(T) * a;
-    if (warps <= 0) return cudaSuccess;
-    long long blocks = (warps + 7) / 8;
+    const long long rows = static_cast<long long>(T) * a;
+    if (rows <= 0) return cudaSuccess;
+    long long blocks = (rows + 63) / 64;  // 8 warps of 8 rows (two steps of 4) per block pass
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     attn_bwd_dot_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(dC, Cc, T, s, a, D);
