@@ -16,6 +16,7 @@
 #include "colsum.cuh"
 #include "dropout.cuh"
 #include "gemm_args.h"
+#include "gemm_plan.h"
 #include "mlp_tp.h"
 #include "sm103_ptx.cuh"
 
@@ -35,18 +36,11 @@ static std::atomic<long long> g_launches{0};
 static void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 // Split tail workspace: room for one fp32 part per unit of up to 160 SMs (a part is a
-// 256 x 512 tile for a CTA pair, at most 128 x 256 for one CTA: 256 KB per SM).
+// 512 x 512 tile for a cluster of four, 256 x 512 for a CTA pair, at most 128 x 256 for one
+// CTA: at most 256 KB per SM).
 constexpr size_t kSplitWsBytes = size_t(160) * 256 * 1024;
-// CTA pairs take 512-wide tiles (25% fewer operand bytes per FLOP than 256-wide; one
-// accumulator, so each tile's epilogue delays the next tile's MMAs by about half an
-// epilogue) when N allows and the K loop is long enough to hide that delay: K >= 2048 for
-// the epilogues that only round the accumulator (+ bias), K >= 4096 for those with math.
-constexpr int kWideMinK = 2048, kWideMinKMath = 4096;
 // 512-wide pair tiles run two pairs per cluster (512 x 512 work tiles, each stage's B fetched
-// once and multicast to both pairs) when the rows make whole 512-row tiles and clusters of
-// four cover at least 90% of the SMs. On a GB300 36 clusters fit (144 of 152 SMs): the
-// multicast saves enough operand traffic that the power-capped clock rises ~5%, more than
-// the idle SMs cost (175b step -2.7%, same-session A/B).
+// once and multicast to both pairs) when gemm_plan.h's rule allows; off, every GEMM uses pairs.
 constexpr bool kClusterPairs = true;
 
 // Clusters of four CTAs of this 512-wide flavour that fit at once, looked up once per SM count.
@@ -62,8 +56,6 @@ static int quad_clusters(int num_sms)
     }
     return clusters;
 }
-// Each part of a split tile runs at least this many 64-deep k blocks.
-constexpr int kMinSplitKb = 16;
 // The split region of a workspace: none when there are no tokens (no GEMM runs then).
 static size_t split_ws_bytes(long long tokens) { return tokens > 0 ? kSplitWsBytes : 0; }
 
@@ -172,96 +164,36 @@ struct SplitOut {
     void* out1 = nullptr;  // G of the bias + GELU epilogue
 };
 
-// The tiles % units tiles of the short last round (all tiles when there are fewer than
-// units) are cut into as many K ranges as keep the parts within one round of units, each
-// of at least kMinSplitKb k blocks, within the workspace; fewer than two parts: no split.
-static void choose_split(GemmArgs& g, long long tiles, int units, int TM, int BN, const SplitOut* so)
-{
-    g.split_tiles = 0;
-    g.split_k = 1;
-    g.split_ws = nullptr;
-    if (!so || !so->ws || !so->out || tiles <= 0 || units <= 1) return;
-    const long long rem = tiles % units;
-    if (rem == 0) return;
-    const int num_kb = (g.K + 63) / 64;
-    long long sk = units / rem;
-    sk = std::min<long long>(sk, num_kb / kMinSplitKb);
-    const size_t part_bytes = static_cast<size_t>(TM) * BN * 4;
-    sk = std::min<long long>(sk, static_cast<long long>(so->ws_bytes / (part_bytes * static_cast<size_t>(rem))));
-    if (sk < 2) return;
-    g.split_tiles = static_cast<int>(rem);
-    g.split_k = static_cast<int>(sk);
-    g.split_ws = so->ws;
-}
-
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const SplitOut* so = nullptr)
 {
     constexpr bool kSplittable = (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU);
-    if (!kSplittable) so = nullptr;
-    // Keep the smaller operand resident in L2 and stream the larger one once: with A
-    // (M*K) no larger than B (N*K), sweep M fastest so every concurrent tile shares one
-    // B block; otherwise sweep N fastest so they share one A block.
-    g.n_fastest = g.M > g.N ? 1 : 0;
-    // Group ~sqrt(units) tiles of the fast dimension: a wave then touches the fewest
-    // distinct operand blocks (DRAM traffic at 18B: 3.8-5.3 GB -> 2.5-2.9 GB per GEMM).
-    const int units = use_pairs(g.M, BN) ? num_sms / 2 : num_sms;
-    g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(units > 1 ? units : 1))));
-    const int wide_min_k = (EPI == EPI_PLAIN || EPI == EPI_BIAS) ? kWideMinK : kWideMinKMath;
-    if (use_pairs(g.M, BN) && g.N % 512 == 0 && g.K >= wide_min_k) BN = 512;
-    const long long tiles_n = (g.N + BN - 1) / BN;
-    g.cluster_pairs = 1;
-    if (kClusterPairs && BN == 512 && ((g.M + 255) / 256) % 2 == 0) {
-        const int quads = std::min(quad_clusters<A_MN, B_MN, EPI>(num_sms), num_sms / 4);
-        if (quads > 0 && 4 * quads * 10 >= 9 * num_sms) {
-            // two CTA pairs per cluster: 512 x 512 work tiles, one cluster per four SMs
-            g.cluster_pairs = 2;
-            g.raster_group = static_cast<int>(std::lround(std::sqrt(static_cast<double>(quads))));
-            const long long tiles = ((g.M + 511) / 512) * tiles_n;
-            choose_split(g, tiles, quads, 512, 512, so);
-            const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
-            const int clusters = static_cast<int>(work < quads ? work : quads);
-            cudaError_t e = launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, 4 * clusters, s);
-            if (e != cudaSuccess) return e;
-            note_launches(1);
-            if (g.split_tiles > 0) {
-                if ((e = launch_splitk_fixup(g, EPI, 512, 512, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) !=
-                    cudaSuccess)
-                    return e;
-                note_launches(1);
-            }
-            return cudaSuccess;
-        }
-    }
-    if (use_pairs(g.M, BN)) {
-        // CTA pairs: 256 x BN tiles, one pair per two SMs.
-        const long long tiles = ((g.M + 255) / 256) * tiles_n;
-        choose_split(g, tiles, num_sms / 2, 256, BN, so);
-        const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
-        const int pairs = static_cast<int>(work < num_sms / 2 ? work : num_sms / 2);
-        cudaError_t e = BN == 512 ? launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s)
-                                  : launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, 2 * pairs, s);
-        if (e != cudaSuccess) return e;
-        note_launches(1);
-        if (g.split_tiles > 0) {
-            if ((e = launch_splitk_fixup(g, EPI, 256, BN, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) != cudaSuccess)
-                return e;
-            note_launches(1);
-        }
-        return cudaSuccess;
-    }
-    const long long tiles = ((g.M + 127) / 128) * tiles_n;
-    choose_split(g, tiles, num_sms, 128, BN, so);
-    const long long work = tiles - g.split_tiles + static_cast<long long>(g.split_tiles) * g.split_k;
-    const int grid = static_cast<int>(work < num_sms ? work : num_sms);
-    if (grid <= 0) return cudaSuccess;
-    cudaError_t e = BN == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, grid, s)
-                              : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, grid, s);
+    constexpr bool kMath = !(EPI == EPI_PLAIN || EPI == EPI_BIAS);
+    if (!kSplittable || !so || !so->ws || !so->out) so = nullptr;
+    int quads = 0;  // looked up only when two-pair clusters are possible
+    if (kClusterPairs && plan_wants_wide(g.M, g.N, g.K, BN, kMath) && ((g.M + 255) / 256) % 2 == 0)
+        quads = quad_clusters<A_MN, B_MN, EPI>(num_sms);
+    const GemmPlan p = plan_gemm(g.M, g.N, g.K, BN, kMath, kSplittable, num_sms, quads, so ? so->ws_bytes : 0);
+    g.n_fastest = p.n_fastest;
+    g.raster_group = p.raster_group;
+    g.cluster_pairs = p.cluster_pairs;
+    g.split_tiles = p.split_tiles;
+    g.split_k = p.split_k;
+    g.split_ws = p.split_tiles > 0 ? so->ws : nullptr;
+    if (p.grid <= 0) return cudaSuccess;
+    cudaError_t e;
+    if (p.cg == 2)
+        e = p.bn == 512 ? launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, p.grid, s)
+                        : launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, p.grid, s);
+    else
+        e = p.bn == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, p.grid, s)
+                        : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, p.grid, s);
     if (e != cudaSuccess) return e;
     note_launches(1);
-    if (g.split_tiles > 0) {
-        if ((e = launch_splitk_fixup(g, EPI, 128, BN, static_cast<__nv_bfloat16*>(so->out), static_cast<__nv_bfloat16*>(so->out1), g.N, s)) != cudaSuccess)
-            return e;
+    if (p.split_tiles > 0) {
+        e = launch_splitk_fixup(g, EPI, p.tm, p.bn, static_cast<__nv_bfloat16*>(so->out),
+                                static_cast<__nv_bfloat16*>(so->out1), g.N, s);
+        if (e != cudaSuccess) return e;
         note_launches(1);
     }
     return cudaSuccess;
