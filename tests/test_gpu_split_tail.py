@@ -147,3 +147,22 @@ def test_attention_split_tails_match_oracle():
     block.attn_step(dev, buf, b, s, a, t, True)
     for k, v in first.items():
         assert torch.equal(v, buf[k]), f"{k} differs between two runs"
+
+
+def test_two_pair_clusters_whole_tiles_match_oracle():
+    """Several whole 512 x 512 work tiles per cluster of two CTA pairs (B multicast): the
+    down-projection and dX are 2 x 36 tiles (two per cluster on a GB300, no split), dA runs on
+    CTA pairs; every output against the full oracle, and bit-for-bit repeatable."""
+    T, h, f, t = 1024, 18432, 2048, 2
+    inp = make_inputs(T, h, f, seed=7, sdy=1.0)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    buf = block.empty_buffers(T, h, f, t)
+    block.step(dev, buf, t)
+    assert _lib.mlp_tp_query_device_status() == 0, _lib.mlp_tp_last_device_where()
+    ref = oracle.fwd_bwd(inp)
+    for k in ("H", "G", "Y", "dX", "dA", "dB", "da", "db"):
+        assert_close(k, buf[k], ref[k])
+    first = {k: buf[k].clone() for k in ("Y", "dX", "dA", "dB")}
+    block.step(dev, buf, t)
+    for k, v in first.items():
+        assert torch.equal(v, buf[k]), f"{k} differs between two runs"
