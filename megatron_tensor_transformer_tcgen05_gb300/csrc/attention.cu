@@ -437,26 +437,29 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
 
 struct DkdvCfg {
     static constexpr int BKV = 128, BQ = 64;
-    static constexpr int THREADS = 320;  // producer, MMA, 8 element-wise warps (two threads per key)
+    // producer, MMA, 16 element-wise warps (four threads per key, 16 queries each)
+    static constexpr int THREADS = 576;
+    static constexpr int EW_WARPS = 16;
     static constexpr int STAGES = 4;                    // Q / dC blocks in flight
     static constexpr uint32_t KT = 128 * kHeadDim * 2;  // K or V block: 32 KB
     static constexpr uint32_t QT = 64 * kHeadDim * 2;   // Q or dC block: 16 KB
+    // per element-wise warp: its 16 queries' L and D (fp32), 128 bytes
     static constexpr uint32_t OFF_K = 0, OFF_V = KT, OFF_QD = 2 * KT, OFF_LD = 2 * KT + STAGES * 2 * QT,
-                              OFF_BAR = OFF_LD + 8 * 2 * 32 * 4;
+                              OFF_BAR = OFF_LD + EW_WARPS * 2 * 16 * 4;
     // barriers: kv | qdofull[4] | qdoempty[4] | stfull[2] | pdfull[2] | dvdkdone[2] | accfull | drain
     static constexpr int NUM_BARS = 1 + 2 * STAGES + 6 + 2;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
     static constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, 128, false, true);
     // S^T[x] at 128x, dP^T[x] at 128x + 64; dV 256; dK 384. P^T and dS^T (bf16 pairs) are
-    // written back over the S^T and dP^T columns each thread has read (queries [32h, 32h+32) at
-    // +32h) and are the A operands of dV += P^T dC and dK += dS^T Q from there.
+    // written back over the S^T and dP^T columns each thread has read (queries [16g, 16g+16) as
+    // 8 columns at +16g) and are the A operands of dV += P^T dC and dK += dS^T Q from there.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DV_COL = 256, DK_COL = 384;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(DkdvCfg::THREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = DkdvCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_stf + 8 * i, 1);
-            mbar_init(b_pdf + 8 * i, 8);
+            mbar_init(b_pdf + 8 * i, C::EW_WARPS);
             mbar_init(b_dvd + 8 * i, 1);
         }
         mbar_init(b_acc, 1);
@@ -582,11 +585,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t qoff = qs * 2 * C::QT, dooff = qoff + C::QT;
-                    // A = P^T and dS^T in TMEM: queries [16k, 16k+16) are 8 columns at +32 (k / 2) + 8 (k % 2)
+                    // A = P^T and dS^T in TMEM: queries [16k, 16k+16) are 8 columns at +16k
 #pragma unroll
                     for (int k = 0; k < C::BQ / 16; ++k) {
                         const uint32_t acc = (pi > 0 || k > 0) ? 1u : 0u;
-                        const uint32_t pa = tmem + 128u * pst + 32u * (k >> 1) + 8u * (k & 1);
+                        const uint32_t pa = tmem + 128u * pst + 16u * k;
                         umma_bf16_tmem_a(tmem + C::DV_COL, pa, desc_at(dQDmn, dooff + 2048u * k), C::IDESC_ACC, acc);
                         umma_bf16_tmem_a(tmem + C::DK_COL, pa + 64u, desc_at(dQDmn, qoff + 2048u * k), C::IDESC_ACC,
                                          acc);
@@ -599,27 +602,30 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
-        // Two threads per key row: warp w (2..9) takes TMEM lane quadrant w % 4 and query
-        // columns [32 half, 32 half + 32) of each 64-query block, half = (w - 2) / 4.
-        const int q = warp & 3, half = (warp - 2) >> 2;
+        // Four threads per key row: warp w (2..17) takes TMEM lane quadrant w % 4 and query
+        // columns [16g, 16g + 16) of each 64-query block, g = (w - 2) / 4.
+        const int q = warp & 3, grp = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int kj = k0 + r;
-        const int cb = 32 * half;
+        const int cb = 16 * grp;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        const uint32_t sL = sLD + static_cast<uint32_t>(warp - 2) * 256u, sD = sL + 128u;
+        const uint32_t sL = sLD + static_cast<uint32_t>(warp - 2) * 128u, sD = sL + 64u;
         const size_t lbase = static_cast<size_t>(bh) * s;
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int st = i & 1;
             const int qq0 = (qb_first + i) * C::BQ + cb;  // this thread's first query column
-            // this warp's 32 values of L and D into its own staging slots
+            // this warp's 16 values of L and D into its own staging slots
             {
                 const int qa = qq0 + lane;
-                const float la = qa < s ? args.lse[lbase + qa] : 0.0f;
-                const float da = qa < s ? args.delta[lbase + qa] : 0.0f;
+                const bool in = lane < 16 && qa < s;
+                const float la = in ? args.lse[lbase + qa] : 0.0f;
+                const float da = in ? args.delta[lbase + qa] : 0.0f;
                 __syncwarp();
-                sts_f32(sL + 4u * lane, la);
-                sts_f32(sD + 4u * lane, da);
+                if (lane < 16) {
+                    sts_f32(sL + 4u * lane, la);
+                    sts_f32(sD + 4u * lane, da);
+                }
                 __syncwarp();
             }
             if (!warp_wait(b_stf + 8 * st, (i >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3005, i)) {
@@ -627,14 +633,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            float p[32], dp[32];
+            float p[16], dp[16];
             {
-                uint32_t u0[32], u1[32];
-                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
-                tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + cb, u1);
+                uint32_t u0[16], u1[16];
+                tmem_ld_32x32b_x16(t_lane + 128u * st + cb, u0);
+                tmem_ld_32x32b_x16(t_lane + 128u * st + 64u + cb, u1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     p[e] = __uint_as_float(u0[e]);
                     dp[e] = __uint_as_float(u1[e]);
                 }
@@ -642,7 +648,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
             const int blk0 = (qb_first + i) * C::BQ;
             const bool need_mask = (args.causal && blk0 < k0 + C::BKV - 1) || blk0 + C::BQ > s || k0 + C::BKV > s;
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
+            for (int c4 = 0; c4 < 4; ++c4) {
                 const float4 L4 = lds128f(sL + 16u * c4), D4 = lds128f(sD + 16u * c4);
                 const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
 #pragma unroll
@@ -657,15 +663,15 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
                     dp[c] = pv * (dp[c] - Dv[e]);
                 }
             }
-            {  // P^T and dS^T over the first 16 of the 32 S^T / dP^T columns this thread has read
-                uint32_t pk[16], dk[16];
+            {  // P^T and dS^T over the first 8 of the 16 S^T / dP^T columns this thread has read
+                uint32_t pk[8], dk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 8; ++e) {
                     pk[e] = pack2_bf16(p[2 * e], p[2 * e + 1]);
                     dk[e] = pack2_bf16(dp[2 * e], dp[2 * e + 1]);
                 }
-                tmem_st_32x32b_x16(t_lane + 128u * st + cb, pk);
-                tmem_st_32x32b_x16(t_lane + 128u * st + 64u + cb, dk);
+                tmem_st_32x32b_x8(t_lane + 128u * st + cb, pk);
+                tmem_st_32x32b_x8(t_lane + 128u * st + 64u + cb, dk);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -675,17 +681,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
         if (ok && nq > 0 && warp_wait(b_acc, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 3007, -1)) {
             tc_fence_after();
             __nv_bfloat16* rowp = args.out + static_cast<size_t>(row0 + kj) * (3 * hd);
-            const int db = 64 * half;  // this thread's half of the d columns of dV and dK
+            const int db = 32 * grp;  // this thread's quarter of the d columns of dV and dK
             uint32_t o[32];
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::DV_COL + db + 32u * c, o);
-                tmem_ld_wait();
-                if (kj < s) store32_global(rowp + colV + db + 32 * c, o, 1.0f);
-                tmem_ld_32x32b_x32(t_lane + C::DK_COL + db + 32u * c, o);
-                tmem_ld_wait();
-                if (kj < s) store32_global(rowp + colK + db + 32 * c, o, args.scale);
-            }
+            tmem_ld_32x32b_x32(t_lane + C::DV_COL + db, o);
+            tmem_ld_wait();
+            if (kj < s) store32_global(rowp + colV + db, o, 1.0f);
+            tmem_ld_32x32b_x32(t_lane + C::DK_COL + db, o);
+            tmem_ld_wait();
+            if (kj < s) store32_global(rowp + colK + db, o, args.scale);
         }
     }
 
@@ -699,7 +702,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dkdv_kernel(const __grid_cons
 
 struct DqCfg {
     static constexpr int BQ = 128, BKV = 64;
-    static constexpr int THREADS = 320;  // producer, MMA, 8 element-wise warps (two threads per query)
+    // producer, MMA, 16 element-wise warps (four threads per query, 16 keys each: four warps
+    // per SM sub-partition hide the latency of each one's ex2 / FMA chains)
+    static constexpr int THREADS = 576;
+    static constexpr int EW_WARPS = 16;
     static constexpr int STAGES = 4;                    // K / V blocks in flight
     static constexpr uint32_t QT = 128 * kHeadDim * 2;  // Q or dC block: 32 KB
     static constexpr uint32_t KT = 64 * kHeadDim * 2;   // K or V block: 16 KB
@@ -710,14 +716,14 @@ struct DqCfg {
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 128, false, true);
     // S[x] at 128x, dP[x] at 128x + 64; dQ at 256. dS_j (bf16 pairs) is written back over the
-    // S_j columns each thread has read (keys [32h, 32h+32) at 128x + 32h) and is the A operand
-    // of dQ += dS_j K_j from there.
+    // S_j columns each thread has read (keys [16g, 16g+16) as 8 columns at 128x + 16g) and is
+    // the A operand of dQ += dS_j K_j from there.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DQ_COL = 256;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnArgs args)
+__global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ AttnArgs args)
 {
     using C = DqCfg;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -753,7 +759,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_spf + 8 * i, 1);
-            mbar_init(b_dsf + 8 * i, 8);
+            mbar_init(b_dsf + 8 * i, C::EW_WARPS);
             mbar_init(b_dqd + 8 * i, 1);
         }
         mbar_init(b_dq, 1);
@@ -839,10 +845,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                     }
                     tc_fence_after();
                     const uint32_t koff = ks * 2 * C::KT;
-                    // A = dS_{pj} in TMEM: keys [16k, 16k+16) are 8 columns at 128 pst + 32 (k / 2) + 8 (k % 2)
+                    // A = dS_{pj} in TMEM: keys [16k, 16k+16) are 8 columns at 128 pst + 16k
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k)
-                        umma_bf16_tmem_a(tmem + C::DQ_COL, tmem + 128u * pst + 32u * (k >> 1) + 8u * (k & 1),
+                        umma_bf16_tmem_a(tmem + C::DQ_COL, tmem + 128u * pst + 16u * k,
                                          desc_at(dKmn, koff + 2048u * k), C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
                     umma_commit(b_kve + 8 * ks);
                     umma_commit(b_dqd + 8 * pst);
@@ -852,12 +858,12 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
             if (!ok && any) drain_mma(b_drain, args.status);
         }
     } else {
-        // Two threads per query row: warp w (2..9) takes TMEM lane quadrant w % 4 and key
-        // columns [32 half, 32 half + 32) of each 64-key block, half = (w - 2) / 4.
-        const int q = warp & 3, half = (warp - 2) >> 2;
+        // Four threads per query row: warp w (2..17) takes TMEM lane quadrant w % 4 and key
+        // columns [16g, 16g + 16) of each 64-key block, g = (w - 2) / 4.
+        const int q = warp & 3, grp = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int qi = q0 + r;
-        const int cb = 32 * half;
+        const int cb = 16 * grp;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const size_t li = static_cast<size_t>(bh) * s + qi;
         const float nLq = qi < s ? -args.lse[li] : 0.0f;
@@ -870,14 +876,14 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                 break;
             }
             tc_fence_after();
-            float p[32], dp[32];
+            float p[16], dp[16];
             {
-                uint32_t u0[32], u1[32];
-                tmem_ld_32x32b_x32(t_lane + 128u * st + cb, u0);
-                tmem_ld_32x32b_x32(t_lane + 128u * st + 64u + cb, u1);
+                uint32_t u0[16], u1[16];
+                tmem_ld_32x32b_x16(t_lane + 128u * st + cb, u0);
+                tmem_ld_32x32b_x16(t_lane + 128u * st + 64u + cb, u1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     p[e] = __uint_as_float(u0[e]);
                     dp[e] = __uint_as_float(u1[e]);
                 }
@@ -885,7 +891,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 16; ++c) {
                 float pv = ex2(fmaf(p[c], args.scale_log2, nLq));
                 if (need_mask) {
                     const int key = kk0 + cb + c;
@@ -893,11 +899,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
                 }
                 dp[c] = pv * (dp[c] - Dq);
             }
-            {  // dS over the first 16 of the 32 S columns this thread has read
-                uint32_t pk[16];
+            {  // dS over the first 8 of the 16 S columns this thread has read
+                uint32_t pk[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack2_bf16(dp[2 * i], dp[2 * i + 1]);
-                tmem_st_32x32b_x16(t_lane + 128u * st + cb, pk);
+                for (int i = 0; i < 8; ++i) pk[i] = pack2_bf16(dp[2 * i], dp[2 * i + 1]);
+                tmem_st_32x32b_x8(t_lane + 128u * st + cb, pk);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -906,15 +912,11 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         if (ok && nkb > 0 && warp_wait(b_dq, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2007, -1)) {
             tc_fence_after();
-            const int db = 64 * half;  // this thread's half of the d columns
-            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0 + qi) * (3 * hd) + colQ + db;
+            const int db = 32 * grp;  // this thread's quarter of the d columns
             uint32_t o[32];
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld_32x32b_x32(t_lane + C::DQ_COL + db + 32u * c, o);
-                tmem_ld_wait();
-                if (qi < s) store32_global(dst + 32 * c, o, args.scale);
-            }
+            tmem_ld_32x32b_x32(t_lane + C::DQ_COL + db, o);
+            tmem_ld_wait();
+            if (qi < s) store32_global(args.out + static_cast<size_t>(row0 + qi) * (3 * hd) + colQ + db, o, args.scale);
         }
     }
 
