@@ -24,8 +24,9 @@
 //   attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key block), looping over 64-query
 //     blocks: S^T = K Q^T, dP^T = V dC^T, P^T = exp2(S^T c - L), dS^T = P^T (dP^T - D) (both
 //     back into TMEM over S^T and dP^T), dV += P^T dC, dK += dS^T Q.
-//   attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query block), looping over 64-key
-//     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D) (back into TMEM over S), dQ += dS K.
+//   attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query block), looping over 128-key
+//     blocks: S = Q K^T, dP = dC V^T, dS = P (dP - D) (into a TMEM double buffer), dQ += dS K;
+//     the next block's S and dP products start as soon as this block's are in registers.
 //   with D = rowsum(dC * C) from attn_bwd_dot_kernel.
 // A tile of Q, K, V or dC is loaded once, row-major with a 128-byte swizzle, and read by
 // the tensor core both as a K-major operand (contraction over d) and as an MN-major one
@@ -701,25 +702,31 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1) attn_bwd_dkdv_kernel(cons
 // ---- backward: dQ ----------------------------------------------------------------------------
 
 struct DqCfg {
-    static constexpr int BQ = 128, BKV = 64;
-    // producer, MMA, 16 element-wise warps (four threads per query, 16 keys each: four warps
-    // per SM sub-partition hide the latency of each one's ex2 / FMA chains)
+    static constexpr int BQ = 128, BKV = 128;  // N = 128 score products
+    // producer, MMA, 16 element-wise warps (four threads per query, 32 keys each)
     static constexpr int THREADS = 576;
     static constexpr int EW_WARPS = 16;
-    static constexpr int STAGES = 4;                    // K / V blocks in flight
+    // K blocks are read by S_j and dQ_j, V blocks by dP_j only: three K slots, freed when
+    // dQ_j completes, and two V slots, freed when dP_j completes, keep the next loads ahead of
+    // the products that wait for them.
+    static constexpr int KSLOTS = 3, VSLOTS = 2;
     static constexpr uint32_t QT = 128 * kHeadDim * 2;  // Q or dC block: 32 KB
-    static constexpr uint32_t KT = 64 * kHeadDim * 2;   // K or V block: 16 KB
-    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_KV = 2 * QT, OFF_BAR = 2 * QT + STAGES * 2 * KT;
-    // barriers: qdo | kvfull[4] | kvempty[4] | spfull[2] | dsfull[2] | dqdone[2] | dqfull | drain
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 6 + 2;
+    static constexpr uint32_t KT = 128 * kHeadDim * 2;  // K or V block: 32 KB
+    static constexpr uint32_t OFF_Q = 0, OFF_DO = QT, OFF_K = 2 * QT, OFF_V = OFF_K + KSLOTS * KT,
+                              OFF_BAR = OFF_V + VSLOTS * KT;
+    // barriers: qdo | kfull[3] | vfull[2] | kempty[3] | vempty[2] | spfull | spread | dsfull[2] |
+    // dqdone[2] | dqfull | drain (the loads' barriers first, for the abort drain)
+    static constexpr int NUM_LOAD_BARS = 1 + KSLOTS + VSLOTS;
+    static constexpr int NUM_BARS = NUM_LOAD_BARS + KSLOTS + VSLOTS + 8;
     static constexpr uint32_t SMEM_BYTES = 1024 + OFF_BAR + 8 * NUM_BARS + 16;
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
     static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, 128, false, true);
-    // S[x] at 128x, dP[x] at 128x + 64; dQ at 256. dS_j (bf16 pairs) is written back over the
-    // S_j columns each thread has read (keys [16g, 16g+16) as 8 columns at 128x + 16g) and is
-    // the A operand of dQ += dS_j K_j from there.
+    // S at 0, dP at 128, dQ at 256; dS_j (bf16 pairs, keys [16k, 16k+16) as 8 columns at
+    // DS_COL + 64 (j % 2) + 8k) double-buffered at 384, the A operand of dQ += dS_j K_j. The
+    // next block's S and dP overwrite this one's as soon as every element-wise warp has loaded
+    // them, so those products run while dS is computed.
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t DQ_COL = 256;
+    static constexpr uint32_t DP_COL = 128, DQ_COL = 256, DS_COL = 384;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -730,10 +737,11 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sKV = base + C::OFF_KV;
+    const uint32_t sQ = base + C::OFF_Q, sdO = base + C::OFF_DO, sK = base + C::OFF_K, sV = base + C::OFF_V;
     const uint32_t bar = base + C::OFF_BAR;
-    const uint32_t b_qdo = bar, b_kvf = bar + 8, b_kve = b_kvf + 8 * C::STAGES, b_spf = b_kve + 8 * C::STAGES,
-                   b_dsf = b_spf + 16, b_dqd = b_dsf + 16, b_dq = b_dqd + 16, b_drain = b_dq + 8;
+    const uint32_t b_qdo = bar, b_kf = bar + 8, b_vf = b_kf + 8 * C::KSLOTS, b_ke = b_vf + 8 * C::VSLOTS,
+                   b_ve = b_ke + 8 * C::KSLOTS, b_spf = b_ve + 8 * C::VSLOTS, b_spr = b_spf + 8, b_dsf = b_spr + 8,
+                   b_dqd = b_dsf + 16, b_dq = b_dqd + 16, b_drain = b_dq + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_BAR + 8 * C::NUM_BARS + 4);
 
@@ -753,12 +761,17 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
 
     if (threadIdx.x == 0) {
         mbar_init(b_qdo, 1);
-        for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(b_kvf + 8 * i, 1);
-            mbar_init(b_kve + 8 * i, 1);
+        for (int i = 0; i < C::KSLOTS; ++i) {
+            mbar_init(b_kf + 8 * i, 1);
+            mbar_init(b_ke + 8 * i, 1);
         }
+        for (int i = 0; i < C::VSLOTS; ++i) {
+            mbar_init(b_vf + 8 * i, 1);
+            mbar_init(b_ve + 8 * i, 1);
+        }
+        mbar_init(b_spf, 1);
+        mbar_init(b_spr, C::EW_WARPS);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(b_spf + 8 * i, 1);
             mbar_init(b_dsf + 8 * i, C::EW_WARPS);
             mbar_init(b_dqd + 8 * i, 1);
         }
@@ -781,7 +794,8 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t issued = 1u, par = 0u;  // drain indices: 0 = qdo, 1 + i = kvfull[i]
+            // drain indices: 0 = qdo, 1 + i = kfull[i], 1 + KSLOTS + i = vfull[i]
+            uint32_t issued = 1u, par = 0u;
             bool ok = true;
             mbar_arrive_expect_tx(b_qdo, 2 * C::QT);
             tma_load_2d(sQ, &args.tmQ, colQ, row0 + q0, b_qdo);
@@ -789,68 +803,89 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
             tma_load_2d(sdO, &args.tmdO, colQ, row0 + q0, b_qdo);
             tma_load_2d(sdO + C::QT / 2, &args.tmdO, colQ + 64, row0 + q0, b_qdo);
             for (int j = 0; j < nkb; ++j) {
-                const int st = j % C::STAGES;
-                const uint32_t ph = static_cast<uint32_t>(j / C::STAGES) & 1u;
-                if (j >= C::STAGES && !mbar_wait_bounded(b_kve + 8 * st, ph ^ 1u, abort_flag, args.status, limit,
+                const int y = row0 + j * C::BKV;
+                // V_j into slot j % 2, free once dP_{j-2} has completed
+                const int vs = j % C::VSLOTS;
+                const uint32_t vph = static_cast<uint32_t>(j / C::VSLOTS) & 1u;
+                if (j >= C::VSLOTS && !mbar_wait_bounded(b_ve + 8 * vs, vph ^ 1u, abort_flag, args.status, limit,
                                                          DEV_TIMEOUT_PRODUCER, 2000, j)) {
                     ok = false;
                     break;
                 }
-                const int y = row0 + j * C::BKV;
-                const uint32_t dk = sKV + st * 2 * C::KT, dv = dk + C::KT, fb = b_kvf + 8 * st;
-                mbar_arrive_expect_tx(fb, 2 * C::KT);
-                tma_load_2d(dk, &args.tmKV, colK, y, fb);
-                tma_load_2d(dk + C::KT / 2, &args.tmKV, colK + 64, y, fb);
-                tma_load_2d(dv, &args.tmKV, colV, y, fb);
-                tma_load_2d(dv + C::KT / 2, &args.tmKV, colV + 64, y, fb);
-                issued |= 1u << (1 + st);
-                par = (par & ~(1u << (1 + st))) | (ph << (1 + st));
+                const uint32_t dv = sV + vs * C::KT, vb = b_vf + 8 * vs;
+                mbar_arrive_expect_tx(vb, C::KT);
+                tma_load_2d(dv, &args.tmKV, colV, y, vb);
+                tma_load_2d(dv + C::KT / 2, &args.tmKV, colV + 64, y, vb);
+                issued |= 1u << (1 + C::KSLOTS + vs);
+                par = (par & ~(1u << (1 + C::KSLOTS + vs))) | (vph << (1 + C::KSLOTS + vs));
+                // K_j into slot j % 3, free once dQ_{j-3} has completed
+                const int ks = j % C::KSLOTS;
+                const uint32_t kph = static_cast<uint32_t>(j / C::KSLOTS) & 1u;
+                if (j >= C::KSLOTS && !mbar_wait_bounded(b_ke + 8 * ks, kph ^ 1u, abort_flag, args.status, limit,
+                                                         DEV_TIMEOUT_PRODUCER, 2008, j)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dk = sK + ks * C::KT, kb = b_kf + 8 * ks;
+                mbar_arrive_expect_tx(kb, C::KT);
+                tma_load_2d(dk, &args.tmKV, colK, y, kb);
+                tma_load_2d(dk + C::KT / 2, &args.tmKV, colK + 64, y, kb);
+                issued |= 1u << (1 + ks);
+                par = (par & ~(1u << (1 + ks))) | (kph << (1 + ks));
             }
-            if (!ok) drain_loads(bar, 1 + C::STAGES, issued, par, args.status);
+            if (!ok) drain_loads(bar, C::NUM_LOAD_BARS, issued, par, args.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = mbar_wait_bounded(b_qdo, 0, abort_flag, args.status, limit, DEV_TIMEOUT_MMA_FULL, 2001, -1);
             bool any = false;
-            const uint64_t dQ = desc_k(sQ), dO = desc_k(sdO), dKV = desc_k(sKV), dKmn = desc_mn(sKV, C::KT / 2);
+            const uint64_t dQ = desc_k(sQ), dO = desc_k(sdO), dK = desc_k(sK), dV = desc_k(sV),
+                           dKmn = desc_mn(sK, C::KT / 2);
             for (int j = 0; ok && j <= nkb; ++j) {
                 if (j < nkb) {  // S_j = Q K_j^T, dP_j = dC V_j^T
-                    const int st = j & 1, ks = j % C::STAGES;
-                    if (!mbar_wait_bounded(b_kvf + 8 * ks, (j / C::STAGES) & 1, abort_flag, args.status, limit,
+                    const int ks = j % C::KSLOTS, vs = j % C::VSLOTS;
+                    if (!mbar_wait_bounded(b_kf + 8 * ks, (j / C::KSLOTS) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, 2002, j) ||
-                        // the buffer held dS_{j-2}, the A operand of dQ_{j-2}
-                        (j >= 2 && !mbar_wait_bounded(b_dqd + 8 * st, ((j - 2) >> 1) & 1, abort_flag, args.status,
-                                                      limit, DEV_TIMEOUT_MMA_ACC, 2003, j))) {
+                        // every element-wise warp has loaded S_{j-1} and dP_{j-1}
+                        (j >= 1 && !mbar_wait_bounded(b_spr, (j - 1) & 1, abort_flag, args.status, limit,
+                                                      DEV_TIMEOUT_MMA_ACC, 2003, j)) ||
+                        !mbar_wait_bounded(b_vf + 8 * vs, (j / C::VSLOTS) & 1, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_FULL, 2006, j)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t koff = ks * 2 * C::KT, voff = koff + C::KT;
+                    const uint32_t koff = ks * C::KT, voff = vs * C::KT;
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint32_t aq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
                         const uint32_t bk = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
-                        umma_bf16(tmem + 128u * st, desc_at(dQ, aq), desc_at(dKV, koff + bk), C::IDESC_S, k > 0);
-                        umma_bf16(tmem + 128u * st + 64u, desc_at(dO, aq), desc_at(dKV, voff + bk), C::IDESC_S, k > 0);
+                        umma_bf16(tmem, desc_at(dQ, aq), desc_at(dK, koff + bk), C::IDESC_S, k > 0);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t aq = (C::QT / 2) * (k >> 2) + 32u * (k & 3);
+                        const uint32_t bk = (C::KT / 2) * (k >> 2) + 32u * (k & 3);
+                        umma_bf16(tmem + C::DP_COL, desc_at(dO, aq), desc_at(dV, voff + bk), C::IDESC_S, k > 0);
                     }
                     any = true;
-                    umma_commit(b_spf + 8 * st);
+                    umma_commit(b_spf);
+                    umma_commit(b_ve + 8 * vs);
                 }
                 if (j >= 1) {  // dQ += dS_{j-1} K_{j-1}
-                    const int pj = j - 1, pst = pj & 1, ks = pj % C::STAGES;
+                    const int pj = j - 1, pst = pj & 1, ks = pj % C::KSLOTS;
                     if (!mbar_wait_bounded(b_dsf + 8 * pst, (pj >> 1) & 1, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_ACC, 2004, pj)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t koff = ks * 2 * C::KT;
-                    // A = dS_{pj} in TMEM: keys [16k, 16k+16) are 8 columns at 128 pst + 16k
+                    const uint32_t koff = ks * C::KT;
 #pragma unroll
                     for (int k = 0; k < C::BKV / 16; ++k)
-                        umma_bf16_tmem_a(tmem + C::DQ_COL, tmem + 128u * pst + 16u * k,
+                        umma_bf16_tmem_a(tmem + C::DQ_COL, tmem + C::DS_COL + 64u * pst + 8u * k,
                                          desc_at(dKmn, koff + 2048u * k), C::IDESC_DQ, (pj > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(b_kve + 8 * ks);
+                    umma_commit(b_ke + 8 * ks);
                     umma_commit(b_dqd + 8 * pst);
                 }
             }
@@ -859,39 +894,43 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
         }
     } else {
         // Four threads per query row: warp w (2..17) takes TMEM lane quadrant w % 4 and key
-        // columns [16g, 16g + 16) of each 64-key block, g = (w - 2) / 4.
+        // columns [32g, 32g + 32) of each 128-key block, g = (w - 2) / 4.
         const int q = warp & 3, grp = (warp - 2) >> 2;
         const int r = 32 * q + lane;
         const int qi = q0 + r;
-        const int cb = 16 * grp;
+        const int cb = 32 * grp;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const size_t li = static_cast<size_t>(bh) * s + qi;
         const float nLq = qi < s ? -args.lse[li] : 0.0f;
         const float Dq = qi < s ? args.delta[li] : 0.0f;
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
-            const int st = j & 1;
-            if (!warp_wait(b_spf + 8 * st, (j >> 1) & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2005, j)) {
+            const int pst = j & 1;
+            if (!warp_wait(b_spf, j & 1, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2005, j)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float p[16], dp[16];
+            float p[32], dp[32];
             {
-                uint32_t u0[16], u1[16];
-                tmem_ld_32x32b_x16(t_lane + 128u * st + cb, u0);
-                tmem_ld_32x32b_x16(t_lane + 128u * st + 64u + cb, u1);
+                uint32_t u0[32], u1[32];
+                tmem_ld_32x32b_x32(t_lane + cb, u0);
+                tmem_ld_32x32b_x32(t_lane + C::DP_COL + cb, u1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 32; ++e) {
                     p[e] = __uint_as_float(u0[e]);
                     dp[e] = __uint_as_float(u1[e]);
                 }
             }
+            // S and dP of this block are in registers: the next block's products may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_spr);
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 float pv = ex2(fmaf(p[c], args.scale_log2, nLq));
                 if (need_mask) {
                     const int key = kk0 + cb + c;
@@ -899,16 +938,23 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
                 }
                 dp[c] = pv * (dp[c] - Dq);
             }
-            {  // dS over the first 8 of the 16 S columns this thread has read
-                uint32_t pk[8];
+            // dS_j goes where dS_{j-2} was: dQ_{j-2} must have read it
+            if (j >= 2 && !warp_wait(b_dqd + 8 * pst, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
+                                     DEV_TIMEOUT_EPILOGUE, 2006, j)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pk[i] = pack2_bf16(dp[2 * i], dp[2 * i + 1]);
-                tmem_st_32x32b_x8(t_lane + 128u * st + cb, pk);
+                for (int i = 0; i < 16; ++i) pk[i] = pack2_bf16(dp[2 * i], dp[2 * i + 1]);
+                tmem_st_32x32b_x16(t_lane + C::DS_COL + 64u * pst + 16u * grp, pk);
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_dsf + 8 * st);
+            if (lane == 0) mbar_arrive(b_dsf + 8 * pst);
         }
         if (ok && nkb > 0 && warp_wait(b_dq, 0, abort_flag, args.status, limit, DEV_TIMEOUT_EPILOGUE, 2007, -1)) {
             tc_fence_after();

@@ -1089,10 +1089,10 @@ extern "C" mlp_status mlp_tp_attn_backward(const mlp_bf16* X, const mlp_bf16* Wq
     note_launches(1);
     timer.mark(MLP_K_ATTN_DOT);
 
-    // dQ: per 128-query block over 64-key blocks.
+    // dQ: per 128-query block over 128-key blocks.
     AttnArgs aq = attn_args(dev, b, s, a, causal);
     if (!make_map(&aq.tmQ, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&aq.tmKV, QKV, 3 * hd, T, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&aq.tmKV, QKV, 3 * hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&aq.tmdO, dC, hd, T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return MLP_ECUDA;
     aq.out = reinterpret_cast<__nv_bfloat16*>(dQKV);
