@@ -133,8 +133,11 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
                            mlp_bf16* dX, mlp_bf16* dA, mlp_bf16* dB, float* da, float* db,
                            void* workspace, size_t workspace_bytes, void* cuda_stream);
 
-/* Bias gradients da = colsum(dH), db = colsum(dY) (fp32, same kernels and results as
- * mlp_tp_backward's) with no workspace and no device allocation of any kind. The paper has
+/* Bias gradients da = colsum(dH), db = colsum(dY) (fp32) with no workspace and no device
+ * allocation of any kind. db is bit for bit mlp_tp_backward's (the same reduction over dY
+ * in the same order). da sums the bf16 dH given here, while mlp_tp_backward's da sums the
+ * dH GEMM's fp32 values before they are rounded, so the two agree to within the bf16
+ * rounding of dH, not bitwise. The paper has
  * no counterpart to this entry point; it exists for callers that cannot allocate device
  * memory when they need these sums: code running inside another runtime that owns all
  * device memory (a framework allocator or fixed arena with nothing to lend), and
