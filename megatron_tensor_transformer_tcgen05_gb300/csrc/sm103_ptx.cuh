@@ -224,6 +224,12 @@ __device__ __forceinline__ void bulk_wait_group()
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+// Start pulling the cache line holding `p` into L2 (an LSU hint; nothing to wait for).
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -100,6 +100,10 @@ struct GemmCfg {
     static constexpr bool DRAIN_FIRST =
         NACC == 1 && EPI_WARPS == 8 && (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU);
     static constexpr uint32_t TMEM_COLS = NACC * BN;                 // fp32 accumulators
+    // 32-column chunks one epilogue warp handles per tile: chunks eset + EPI_SETS * k
+    static constexpr int NCH = OBN / 32 / EPI_SETS;
+    static constexpr bool HAS_BIAS = (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_DROPOUT_RES);
+    static constexpr bool DGELU_ANY = (EPI == EPI_DGELU || EPI == EPI_DGELU_G);
     // as many stages as fit beside the epilogue staging (at most 6 for pairs, 4 alone)
     static constexpr int STAGES_FIT = static_cast<int>((232448u - 1024u - 256u - EPI_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT < ((CG == 2) ? 6 : 4) ? STAGES_FIT : ((CG == 2) ? 6 : 4);
@@ -111,6 +115,7 @@ struct GemmCfg {
     static_assert(BN == 128 || BN == 256 || BN == 512, "tile width");
     static_assert(CG == 1 ? BN <= 256 : (BN == 256 || (BN == 512 && !DUAL)), "CTA pairs use 256- or 512-wide tiles");
     static_assert(TMEM_COLS <= 512, "tensor memory columns");
+    static_assert(!HAS_BIAS || (NCH >= 1 && NCH <= 8), "a warp's bias values fit one 16-byte load per lane");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(STAGES >= 3, "pipeline depth");
     static_assert(!DUAL || (B_MN && BN == 256), "dual B operand: MN-major, 256-wide MMA");
@@ -119,40 +124,104 @@ struct GemmCfg {
 // In-flight copies get this long to land after an abort before the CTA exits.
 constexpr unsigned long long kDrainLimitNs = 2000000000ull;
 
+// ---- packed fp32 pairs --------------------------------------------------------------------
+// The sm_100-family f32x2 fma / mul / add do two IEEE round-to-nearest operations in one
+// instruction; a pair lives in one 64-bit register.
+typedef unsigned long long f32x2_t;
+
+__device__ __forceinline__ f32x2_t f2_pack(float lo, float hi)
+{
+    f32x2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2_t f2_splat(float k) { return f2_pack(k, k); }
+__device__ __forceinline__ f32x2_t f2_fma(f32x2_t a, f32x2_t b, f32x2_t c)
+{
+    f32x2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2_t f2_mul(f32x2_t a, f32x2_t b)
+{
+    f32x2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float ex2_approx(float z)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
+    return r;
+}
+
+// GELU, tanh form, on a pair of values. With u = sqrt(2/pi) (x + 0.044715 x^3):
+//   1 + tanh u = 2 s,  s = sigmoid(2u) = 1 / (1 + e),  e = exp(-2u),
+//   GELU(x) = x s,     GELU'(x) = s + 2 x s (1 - s) u'(x),  u'(x) = sqrt(2/pi) (1 + 3 0.044715 x^2).
+// e = 2^z with z = -2 log2(e) u = x (c0 + c1 x^2): one special-function op per value. The
+// reciprocal 1 / (1 + e) runs on the FMA pipe: Newton's iteration r <- r + r (1 - d r) from
+// the integer estimate bits(r0) = R - bits(d), R = 0x7EF311C0 (chosen by search over all
+// mantissas: |r0 d - 1| <= 5.06% for every normal d); three steps leave <= 1 ulp. Since
+// 1 - s = e s, s (1 - s) = s^2 e has no cancellation. z is capped at 120 (s < 1e-36 there),
+// so d and r0 stay normal numbers.
+struct GeluPair {
+    f32x2_t x, x2, e, s;
+};
+
+__device__ __forceinline__ GeluPair gelu_sigmoid_pair(f32x2_t x)
+{
+    constexpr float kC0 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654);
+    constexpr float kC1 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
+    GeluPair g;
+    g.x = x;
+    g.x2 = f2_mul(x, x);
+    float z0, z1;
+    f2_unpack(f2_mul(x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
+    g.e = f2_pack(ex2_approx(fminf(z0, 120.0f)), ex2_approx(fminf(z1, 120.0f)));
+    const f32x2_t nd = f2_fma(g.e, f2_splat(-1.0f), f2_splat(-1.0f));  // -(1 + e)
+    float d0, d1;
+    f2_unpack(nd, d0, d1);
+    // bits(-(1 + e)) = bits(1 + e) + 2^31, so R - bits(1 + e) = (R + 2^31) - bits(-(1 + e))
+    f32x2_t r = f2_pack(__uint_as_float(0xFEF311C0u - __float_as_uint(d0)),
+                        __uint_as_float(0xFEF311C0u - __float_as_uint(d1)));
+    const f32x2_t one = f2_splat(1.0f);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) r = f2_fma(r, f2_fma(nd, r, one), r);
+    g.s = r;
+    return g;
+}
+
+__device__ __forceinline__ f32x2_t gelu_value_pair(const GeluPair& g) { return f2_mul(g.x, g.s); }
+
+__device__ __forceinline__ f32x2_t gelu_grad_pair(const GeluPair& g)
+{
+    constexpr float kD0 = static_cast<float>(2.0 * 0.7978845608028654);
+    constexpr float kD1 = static_cast<float>(2.0 * 0.7978845608028654 * 3.0 * 0.044715);
+    const f32x2_t w = f2_mul(g.x, f2_fma(g.x2, f2_splat(kD1), f2_splat(kD0)));  // 2 x u'(x)
+    const f32x2_t q = f2_mul(f2_mul(g.s, g.s), g.e);                            // s (1 - s)
+    return f2_fma(q, w, g.s);
+}
+
+// Scalar forms (the split-tail fixup): the pair code on (x, x), so every path gets the same bits.
 __device__ __forceinline__ float gelu_tanh_f(float x)
 {
-    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-    const float u = k0 * x * fmaf(k1, x * x, 1.0f);
-    const float e = __expf(-2.0f * u);
-    return x * __fdividef(1.0f, 1.0f + e);  // x * sigmoid(2u)
+    float lo, hi;
+    f2_unpack(gelu_value_pair(gelu_sigmoid_pair(f2_pack(x, x))), lo, hi);
+    return lo;
 }
-
-// d/dx of the tanh form with s = sigmoid(2u): 1 + tanh u = 2s and 1 - tanh^2 u = 4 s (1 - s),
-// so GELU'(x) = s + 2 x s (1 - s) u'(x), u'(x) = sqrt(2/pi) (1 + 3 * 0.044715 x^2).
 __device__ __forceinline__ float gelu_tanh_grad_f(float x)
 {
-    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-    const float x2 = x * x;
-    const float u = k0 * x * fmaf(k1, x2, 1.0f);
-    const float e = __expf(-2.0f * u);
-    const float s = __fdividef(1.0f, 1.0f + e);
-    const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
-    return fmaf(2.0f * x * s * (1.0f - s), du, s);
+    float lo, hi;
+    f2_unpack(gelu_grad_pair(gelu_sigmoid_pair(f2_pack(x, x))), lo, hi);
+    return lo;
 }
 
-// GELU'(x) as gelu_tanh_grad_f (same operations, so the same bits), and GELU(x) in g from
-// the same sigmoid, as gelu_tanh_f computes it.
-__device__ __forceinline__ float gelu_tanh_grad_and_value_f(float x, float& g)
-{
-    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-    const float x2 = x * x;
-    const float u = k0 * x * fmaf(k1, x2, 1.0f);
-    const float e = __expf(-2.0f * u);
-    const float s = __fdividef(1.0f, 1.0f + e);
-    g = x * s;
-    const float du = k0 * fmaf(3.0f * k1, x2, 1.0f);
-    return fmaf(2.0f * x * s * (1.0f - s), du, s);
-}
+// G = GELU of the bf16 pair packed in w (low half first), rounded to a bf16 pair.
+__device__ __forceinline__ uint32_t gelu_bf16x2(uint32_t w);
 
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
@@ -168,6 +237,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t gelu_bf16x2(uint32_t w)
+{
+    float g0, g1;
+    f2_unpack(gelu_value_pair(gelu_sigmoid_pair(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)))), g0,
+              g1);
+    return pack_bf16x2(g0, g1);
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* out)
@@ -224,6 +301,22 @@ __device__ __forceinline__ void stage_row_sw64(uint32_t buf, int lane, const uin
 #pragma unroll
     for (uint32_t j = 0; j < 4; ++j)
         sts_v4(row + ((j ^ x) << 4), p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+}
+
+// Bias of chunk wc of this warp: before the tile's accumulator is ready, lane l loads the 8
+// bias values of columns [8 (l % 4), +8) of chunk l / 4 as one 16-byte word (bw); here each
+// lane takes the 32 values of chunk wc from lanes 4 wc .. 4 wc + 3 by shuffles and adds
+// them to its row. Shuffles instead of a load per chunk: the loads' latency would otherwise
+// sit between reading the accumulator out of TMEM and releasing it.
+__device__ __forceinline__ void add_bias_chunk(float (&v)[32], const uint4& bw, int wc)
+{
+#pragma unroll
+    for (int jp = 0; jp < 16; ++jp) {
+        const uint32_t w = (jp & 3) == 0 ? bw.x : (jp & 3) == 1 ? bw.y : (jp & 3) == 2 ? bw.z : bw.w;
+        const uint32_t x = __shfl_sync(0xffffffffu, w, 4 * wc + (jp >> 2));
+        v[2 * jp] += __uint_as_float(x << 16);
+        v[2 * jp + 1] += __uint_as_float(x & 0xFFFF0000u);
+    }
 }
 
 // Output tile `tile` -> its first row and column. Tiles that run at the same time (about
@@ -569,6 +662,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
         for (int u = unit; u < num_work; u += num_units) {
             int tile, kb_lo, kb_hi, part;
             work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
+            int m0, n0;
+            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
+            const int row_blk = m0 + prow + C::BM * static_cast<int>(rank) + 32 * q;
+            const int row = row_blk + lane;
+            // While the tile's main loop still runs: this warp's bias values (add_bias_chunk)
+            // and, for the GELU' epilogues, this lane's row of H for its first three chunks
+            // pulled into L2 (then each chunk pulls in the one three ahead).
+            uint4 bias_w = make_uint4(0, 0, 0, 0);
+            if (C::HAS_BIAS && part < 0) {
+                const int wc = lane >> 2;
+                const int n = n0 + 32 * (eset + C::EPI_SETS * wc) + 8 * (lane & 3);
+                if (wc < C::NCH && n < N) bias_w = ldg_nc_v4(args.bias + n);
+            }
+            if (C::DGELU_ANY && part < 0 && row < M) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int n = n0 + 32 * (eset + C::EPI_SETS * k);
+                    if (k < C::NCH && n < N) prefetch_l2(args.aux + static_cast<size_t>(row) * args.ld_aux + n);
+                }
+            }
             // One lane waits; the warp follows its verdict so the .sync.aligned TMEM loads
             // below always run with all 32 lanes.
             int ready = 0;
@@ -578,10 +691,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             ready = __shfl_sync(0xffffffffu, ready, 0);
             if (!ready) break;
             tc_fence_after();
-            int m0, n0;
-            tile_origin(tile, tiles_m, tiles_n, args.n_fastest, args.raster_group, TM, C::OBN, m0, n0);
-            const int row_blk = m0 + prow + C::BM * static_cast<int>(rank) + 32 * q;
-            const int row = row_blk + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
             // a part of a split tile: its fp32 accumulator, chunk c of 32 columns at
             // [c][row within the tile][32] of this part's TM x OBN block of split_ws
@@ -590,6 +699,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 part_out = args.split_ws + static_cast<size_t>(part) * TM * C::OBN +
                            static_cast<size_t>(prow + C::BM * static_cast<int>(rank) + 32 * q + lane) * 32;
 
+            // hnext: the aux row segment of this warp's next chunk (H, the residual, Ha);
+            // gnext: Hg.
             uint4 hnext[4], gnext[4];
             if (EPI == EPI_DGELU || EPI == EPI_DGELU_G || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
 #pragma unroll
@@ -619,17 +730,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                        if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                float bv[8];
-                                const int n = nc + 8 * i;
-                                const uint4 u = n < N ? ldg_nc_v4(args.bias + n) : make_uint4(0, 0, 0, 0);
-                                unpack_bf16x8(u, bv);
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) v[8 * i + j] += bv[j];
-                            }
-                        }
+                        if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) add_bias_chunk(v, bias_w, hh * KPH + k);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) pk[k][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                     }
@@ -649,11 +750,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         uint32_t p1[16];
                         if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float h0 = __uint_as_float(pk[k][j] << 16);
-                                const float h1 = __uint_as_float(pk[k][j] & 0xFFFF0000u);
-                                p1[j] = pack_bf16x2(gelu_tanh_f(h0), gelu_tanh_f(h1));
-                            }
+                            for (int j = 0; j < 16; ++j) p1[j] = gelu_bf16x2(pk[k][j]);
                         }
                         const uint32_t buf0 = s_epi + ((ewarp * C::STG_BUFS + sel) * C::NOUT) * C::STG_BYTES;
                         if (lane == 0) bulk_wait_group_read<C::STG_BUFS - 1>();  // its last store has read it
@@ -672,7 +769,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
             } else
 #pragma unroll 1
-            for (int c = eset; c < C::OBN / 32; c += C::EPI_SETS) {
+            for (int c = eset, wc = 0; c < C::OBN / 32; c += C::EPI_SETS, ++wc) {
                 const int nc = n0 + 32 * c;
                 const bool active = nc < N;  // warp-uniform
                 uint32_t r[32], r2[32];
@@ -746,17 +843,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         v[2 * j + 1] = d1 * hg[2 * j + 1] * silu_grad_f(ha[2 * j + 1]);
                     }
                 }
-                if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_DROPOUT_RES) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float bv[8];
-                        const int n = nc + 8 * i;
-                        const uint4 u = n < N ? ldg_nc_v4(args.bias + n) : make_uint4(0, 0, 0, 0);
-                        unpack_bf16x8(u, bv);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[8 * i + j] += bv[j];
-                    }
-                }
+                if (C::HAS_BIAS) add_bias_chunk(v, bias_w, wc);
                 if (EPI == EPI_BIAS_DROPOUT_RES) {
                     float rv[32];
 #pragma unroll
@@ -780,11 +867,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                             v[4 * g + w] = rv[4 * g + w] + (((kb >> w) & 1u) ? v[4 * g + w] * args.drop.scale : 0.0f);
                     }
                 }
+                float cs0 = 0.0f;  // GELU' epilogues: column sum of this warp's 32 rows, column nc + lane
                 if (EPI == EPI_DGELU || EPI == EPI_DGELU_G) {
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
-                    if (c + C::EPI_SETS < C::OBN / 32) {  // prefetch the next chunk of H
+                    if (c + C::EPI_SETS < C::OBN / 32) {  // the next chunk of H into registers
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int n = nc + 32 * C::EPI_SETS + 8 * i;
@@ -793,32 +881,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                                            : make_uint4(0, 0, 0, 0);
                         }
                     }
-                    if (EPI == EPI_DGELU_G) {
-                        float gv[32];
+                    if (c + 3 * C::EPI_SETS < C::OBN / 32 && row < M && nc + 96 * C::EPI_SETS < N)  // and three ahead into L2
+                        prefetch_l2(args.aux + static_cast<size_t>(row) * args.ld_aux + nc + 96 * C::EPI_SETS);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_and_value_f(hv[j], gv[j]);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) p1[j] = pack_bf16x2(gv[2 * j], gv[2 * j + 1]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= gelu_tanh_grad_f(hv[j]);
+                    for (int j = 0; j < 16; ++j) {  // dH = dG GELU'(H), two columns at a time
+                        const GeluPair gp = gelu_sigmoid_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
+                        f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), gelu_grad_pair(gp)), v[2 * j], v[2 * j + 1]);
+                        if (EPI == EPI_DGELU_G) {  // and G = GELU(H) from the same sigmoid
+                            float g0, g1;
+                            f2_unpack(gelu_value_pair(gp), g0, g1);
+                            p1[j] = pack_bf16x2(g0, g1);
+                        }
                     }
                     if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
                         float cs[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) cs[j] = v[j];
                         warp_column_sums(cs, lane);
-                        if (nc + lane < N)
-                            args.colsum_rows[static_cast<size_t>(row_blk >> 5) * N + nc + lane] = cs[0];
+                        cs0 = cs[0];
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                 if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H, as in every path
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        p1[j] = pack_bf16x2(gelu_tanh_f(__uint_as_float(p0[j] << 16)),
-                                            gelu_tanh_f(__uint_as_float(p0[j] & 0xFFFF0000u)));
+                    for (int j = 0; j < 16; ++j) p1[j] = gelu_bf16x2(p0[j]);
                 }
 
                 const uint32_t buf0 = s_epi + ((ewarp * C::STG_BUFS + sel) * C::NOUT) * C::STG_BYTES;
@@ -836,6 +923,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     bulk_commit_group();
                 }
                 if (C::STG_BUFS == 2) sel ^= 1u;
+                // the column sums go out after the staging fence and the store
+                if ((EPI == EPI_DGELU || EPI == EPI_DGELU_G) && args.colsum_rows && nc + lane < N)
+                    args.colsum_rows[static_cast<size_t>(row_blk >> 5) * N + nc + lane] = cs0;
             }
             if (C::NACC == 2) {
                 acc ^= 1u;
