@@ -89,7 +89,7 @@ struct GemmCfg {
     // Epilogue warps: 8 (two per TMEM lane quadrant, taking alternate 32-column chunks) for the
     // one-accumulator 512-wide tiles, whose epilogue holds up the next tile's MMAs until each
     // half is read out; else 4. With 8, each warp stages through one buffer instead of two.
-    static constexpr int EPI_WARPS = (NACC == 1 && EPI != EPI_DGELU_G) ? 8 : 4;
+    static constexpr int EPI_WARPS = (NACC == 1) ? 8 : 4;
     static constexpr int EPI_SETS = EPI_WARPS / 4;
     static constexpr int STG_BUFS = EPI_WARPS == 8 ? 1 : 2;
     static constexpr uint32_t EPI_BYTES = EPI_WARPS * STG_BUFS * NOUT * STG_BYTES;
