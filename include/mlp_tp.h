@@ -187,15 +187,28 @@ size_t mlp_tp_swiglu_workspace_bytes(int T, int h, int f, int t);
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t);
 
 /* GELU recompute ("Efficient Large-Scale Language Model Training ... Megatron-LM", section 3
- * "Activation Recomputation": keep fewer activations, recompute them in the backward). The
- * backward of the block when the forward's G was not kept: the caller may pass the forward
- * any scratch buffer for G (one shared by every layer) and keep only H. The dH GEMM's
- * epilogue recomputes G = GELU(H) from the stored bf16 H (from the sigmoid GELU' needs
- * anyway) into the workspace, and dB = G^T dY reads it there. The forward computes G from
- * the rounded H too, so the recomputed G and every gradient are bitwise those of
- * mlp_tp_backward. Workspace (256-byte aligned, at least mlp_tp_recompute_workspace_bytes):
- * dH [T,f] bf16 | G [T,f] bf16 | the reduction partials | split-tail parts; dH and G are
- * there on return. Other arguments and errors as mlp_tp_backward. */
+ * "Activation Recomputation": keep fewer activations, recompute them in the backward; and
+ * "Distributed training", section 2.2: the MLP's saved activations are the GELU input and
+ * the down-projection input). G = GELU(H) is never stored:
+ *   mlp_tp_forward_recompute  writes H = X*A + a (first GEMM, bias epilogue) and
+ *       Y = GELU(H)*B + b: the second GEMM reads H, and operand-transform warps turn each
+ *       landed H tile into G in shared memory before its MMAs (the same arithmetic as the
+ *       GELU epilogue of mlp_tp_forward, so Y is bitwise mlp_tp_forward's when H is; the
+ *       first GEMM is tiled as in mlp_tp_forward, so it is). Arguments, workspace and errors
+ *       as mlp_tp_forward, without G.
+ *   mlp_tp_backward_recompute  the backward from the kept H alone: dB = GELU(H)^T dY reads H
+ *       with the same on-chip transform; every gradient is bitwise mlp_tp_backward's with the
+ *       forward's G. Workspace: mlp_tp_recompute_workspace_bytes (= mlp_tp_workspace_bytes),
+ *       with dH in its first T*f*2 bytes on return. Other arguments and errors as
+ *       mlp_tp_backward.
+ * The transform costs about 8 GELU evaluations per clock per SM next to the MMAs (one A value
+ * per 512 multiply-adds of a 512-wide tile, every A tile once per output-column tile), so
+ * these two GEMMs run slower than the ones that read a stored G; what they save is the G
+ * activation ([T,f] bf16) and its HBM traffic. */
+mlp_status mlp_tp_forward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
+                                    const mlp_bf16* B, const mlp_bf16* b, int T, int h, int f, int t,
+                                    mlp_bf16* H, mlp_bf16* Y, void* workspace, size_t workspace_bytes,
+                                    void* cuda_stream);
 size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t);
 mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
                                      const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX, mlp_bf16* dA,

@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
             L.mlp_tp_recompute_workspace_bytes.argtypes = [i32] * 4
             L.mlp_tp_backward_recompute.restype = i32
             L.mlp_tp_backward_recompute.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 5 + [vp, sz, vp]
+            L.mlp_tp_forward_recompute.restype = i32
+            L.mlp_tp_forward_recompute.argtypes = [vp] * 5 + [i32] * 4 + [vp] * 2 + [vp, sz, vp]
             _lib = L
     return _lib
 
@@ -245,6 +247,12 @@ def mlp_tp_attn_backward(X, Wqkv, Wo, QKV, C, L, dY, b: int, s: int, h: int, a: 
     _check(lib().mlp_tp_attn_backward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(QKV), _ptr(C), _ptr(L), _ptr(dY), b, s, h,
                                       a, d, t, int(bool(causal)), _ptr(dX), _ptr(dWqkv), _ptr(dWo), _ptr(workspace),
                                       workspace_bytes, _stream(stream)), "mlp_tp_attn_backward")
+
+
+def mlp_tp_forward_recompute(X, A, a, B, b, T: int, h: int, f: int, t: int, H, Y, workspace, workspace_bytes: int,
+                             stream=None) -> None:
+    _check(lib().mlp_tp_forward_recompute(_ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), T, h, f, t, _ptr(H), _ptr(Y),
+                                          _ptr(workspace), workspace_bytes, _stream(stream)), "mlp_tp_forward_recompute")
 
 
 def mlp_tp_recompute_workspace_bytes(T: int, h: int, f: int, t: int) -> int:

@@ -17,7 +17,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmlp_tp.so")
 
 SOURCES = ["mlp_tp_api.cu", "gemm_fwd_up.cu", "gemm_fwd_down.cu", "gemm_bwd_dh.cu",
-           "gemm_bwd_dx.cu", "gemm_bwd_dw.cu", "gemm_swiglu.cu", "gemm_splitk.cu", "attention.cu"]
+           "gemm_bwd_dx.cu", "gemm_bwd_dw.cu", "gemm_swiglu.cu", "gemm_splitk.cu", "gemm_recompute.cu",
+           "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr"]

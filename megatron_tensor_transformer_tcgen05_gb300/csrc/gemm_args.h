@@ -16,7 +16,10 @@ enum Epi : int {
     EPI_BIAS_DROPOUT_RES = 4,
     EPI_SWIGLU = 5,   // dual B operand: D = [X A | X Wg] per 128 output columns -> Ha, Hg, U
     EPI_DSWIGLU = 6,  // dU = acc; dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha) -> dHa, dHg
-    EPI_DGELU_G = 7,  // as EPI_DGELU, and G = GELU(H) recomputed from the same sigmoid -> dH, G
+    // The A operand is H, turned into G = GELU(H) in shared memory before the MMAs read it
+    // (operand-transform warps); the epilogue is that of EPI_PLAIN / EPI_BIAS.
+    EPI_PLAIN_GA = 8,
+    EPI_BIAS_GA = 9,
 };
 
 struct GemmArgs {

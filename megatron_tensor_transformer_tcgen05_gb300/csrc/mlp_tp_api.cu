@@ -164,11 +164,18 @@ struct SplitOut {
     void* out1 = nullptr;  // G of the bias + GELU epilogue
 };
 
+// tiles_as_math: plan the tile shapes as for an epilogue with math (-1: by EPI). The GELU
+// recompute's up-projection (bias only) takes the bias + GELU GEMM's plan, so that its H is
+// bitwise the H of the forward that keeps G.
 template <bool A_MN, bool B_MN, int EPI>
-static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const SplitOut* so = nullptr)
+static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const SplitOut* so = nullptr,
+                        int tiles_as_math = -1)
 {
-    constexpr bool kSplittable = (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU);
-    constexpr bool kMath = !(EPI == EPI_PLAIN || EPI == EPI_BIAS);
+    // the transform flavours finish like their plain / bias epilogue
+    constexpr int kEpiB = (EPI == EPI_PLAIN_GA) ? EPI_PLAIN : (EPI == EPI_BIAS_GA) ? EPI_BIAS : EPI;
+    constexpr bool kSplittable =
+        (kEpiB == EPI_PLAIN || kEpiB == EPI_BIAS || kEpiB == EPI_BIAS_GELU || kEpiB == EPI_DGELU);
+    const bool kMath = tiles_as_math >= 0 ? tiles_as_math != 0 : !(kEpiB == EPI_PLAIN || kEpiB == EPI_BIAS);
     if (!kSplittable || !so || !so->ws || !so->out) so = nullptr;
     int quads = 0;  // looked up only when two-pair clusters are possible
     if (kClusterPairs && plan_wants_wide(g.M, g.N, g.K, BN, kMath) && ((g.M + 255) / 256) % 2 == 0)
@@ -191,7 +198,7 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     if (e != cudaSuccess) return e;
     note_launches(1);
     if (p.split_tiles > 0) {
-        e = launch_splitk_fixup(g, EPI, p.tm, p.bn, static_cast<__nv_bfloat16*>(so->out),
+        e = launch_splitk_fixup(g, kEpiB, p.tm, p.bn, static_cast<__nv_bfloat16*>(so->out),
                                 static_cast<__nv_bfloat16*>(so->out1), g.N, s);
         if (e != cudaSuccess) return e;
         note_launches(1);
@@ -310,19 +317,19 @@ const char* mlp_tp_status_string(mlp_status s)
 
 // Backward workspace: dH [T,f] bf16 | dH column sums per 32-row block [ceil(T/32), f] fp32 |
 // dY column sums per row slice [slices, h] fp32 | split-tail parts (kSplitWsBytes), each
-// region 256-byte aligned. The recompute backward puts G [T,f] bf16 right after dH.
+// region 256-byte aligned. The recompute backward uses the same layout (G is never stored).
 static size_t ws_dh_bytes(int T, int f) { return round256(static_cast<size_t>(T) * f * 2); }
 static size_t ws_rows_bytes(int T, int f) { return round256(static_cast<size_t>((T + 31) / 32) * f * 4); }
 static size_t ws_dy_bytes(int T, int h) { return round256(static_cast<size_t>(colsum_splits(T)) * h * 4); }
-static size_t bwd_ws_before_split(int T, int h, int f, bool recompute)
+static size_t bwd_ws_before_split(int T, int h, int f)
 {
-    return (recompute ? 2 : 1) * ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
+    return ws_dh_bytes(T, f) + ws_rows_bytes(T, f) + ws_dy_bytes(T, h);
 }
 
 size_t mlp_tp_workspace_bytes(int T, int h, int f, int t)
 {
     if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    return bwd_ws_before_split(T, h, f, false) + split_ws_bytes(T);
+    return bwd_ws_before_split(T, h, f) + split_ws_bytes(T);
 }
 
 size_t mlp_tp_forward_workspace_bytes(void) { return kSplitWsBytes; }
@@ -334,16 +341,18 @@ long long mlp_tp_launch_count(void) { return g_launches.load(std::memory_order_r
 namespace mlp {
 
 // The forward pass; with `drop` set, GEMM 2's epilogue also applies dropout and adds the
-// residual R, writing Z instead of Y.
+// residual R, writing Z instead of Y. With G == NULL (the GELU recompute), GEMM 1 stores H
+// alone and GEMM 2 reads H, turning each A tile into G = GELU(H) in shared memory.
 static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
                                const mlp_bf16* b, const mlp_bf16* R, const DropoutParams* drop, int T, int h,
                                int f, int t, mlp_bf16* H, mlp_bf16* G, mlp_bf16* Y, void* workspace,
                                size_t workspace_bytes, void* cuda_stream)
 {
+    const bool recompute = (G == nullptr);
     mlp_status st = check_shape(T, h, f, t);
     if (st != MLP_OK) return st;
     // Token-indexed buffers may be NULL only when there are no tokens.
-    if (!A || !a || !B || !b || (T > 0 && (!X || !H || !G || !Y || (drop && !R)))) return MLP_EINVAL;
+    if (!A || !a || !B || !b || (T > 0 && (!X || !H || !Y || (drop && !R)))) return MLP_EINVAL;
     const void* ptrs[] = {X, A, a, B, b, H, G, Y, R};
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
@@ -357,23 +366,27 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     CallTimer timer(s);
 
-    // GEMM 1: H = X*A + a, G = GELU(H). N-tiles never straddle a shard when f/t % BN == 0.
+    // GEMM 1: H = X*A + a, G = GELU(H) (H alone when recomputing). N-tiles never straddle a
+    // shard when f/t % BN == 0.
     GemmArgs g1{};
     if (!map_kmajor(&g1.tmA, X, h, T, 128) || !map_mnmajor(&g1.tmB, A, f, h) ||
-        !map_store(&g1.tmD0, H, f, T) || !map_store(&g1.tmD1, G, f, T))
+        !map_store(&g1.tmD0, H, f, T) || (!recompute && !map_store(&g1.tmD1, G, f, T)))
         return MLP_ECUDA;
+    if (recompute) g1.tmD1 = g1.tmD0;
     g1.M = T; g1.N = f; g1.K = h;
     g1.bias = reinterpret_cast<const __nv_bfloat16*>(a);
     g1.status = dev->status;
     g1.timeout_ns = kWaitLimitNs;
     const SplitOut so1{static_cast<float*>(workspace), workspace ? workspace_bytes : 0, H, G};
-    if (gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s, &so1) != cudaSuccess) return MLP_ECUDA;
+    const cudaError_t e1 = recompute ? gemm<false, true, EPI_BIAS>(g1, bn_f, dev->num_sms, s, &so1, 1)
+                                     : gemm<false, true, EPI_BIAS_GELU>(g1, bn_f, dev->num_sms, s, &so1);
+    if (e1 != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_FWD_UP);
 
     // GEMM 2: Y = sum over shards of G_i*B_i, + b (then dropout and + R). One accumulator
-    // over K = f.
+    // over K = f. Recomputing: the A operand is H, and G = GELU(H) is formed on chip.
     GemmArgs g2{};
-    if (!map_kmajor(&g2.tmA, G, f, T, 128) || !map_mnmajor(&g2.tmB, B, h, f) ||
+    if (!map_kmajor(&g2.tmA, recompute ? H : G, f, T, 128) || !map_mnmajor(&g2.tmB, B, h, f) ||
         !map_store(&g2.tmD0, Y, h, T))
         return MLP_ECUDA;
     g2.tmD1 = g2.tmD0;
@@ -387,6 +400,8 @@ static mlp_status forward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_b
         g2.ld_aux = h;
         g2.drop = *drop;
         e = gemm<false, true, EPI_BIAS_DROPOUT_RES>(g2, bn_h, dev->num_sms, s);
+    } else if (recompute) {
+        e = gemm<false, true, EPI_BIAS_GA>(g2, bn_h, dev->num_sms, s, &so);
     } else {
         e = gemm<false, true, EPI_BIAS>(g2, bn_h, dev->num_sms, s, &so);
     }
@@ -415,7 +430,16 @@ mlp_status mlp_tp_forward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* 
                           const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* G,
                           mlp_bf16* Y, void* workspace, size_t workspace_bytes, void* cuda_stream)
 {
+    if (T > 0 && !G) return MLP_EINVAL;
     return forward_impl(X, A, a, B, b, nullptr, nullptr, T, h, f, t, H, G, Y, workspace, workspace_bytes,
+                        cuda_stream);
+}
+
+mlp_status mlp_tp_forward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B,
+                                    const mlp_bf16* b, int T, int h, int f, int t, mlp_bf16* H, mlp_bf16* Y,
+                                    void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    return forward_impl(X, A, a, B, b, nullptr, nullptr, T, h, f, t, H, nullptr, Y, workspace, workspace_bytes,
                         cuda_stream);
 }
 
@@ -427,6 +451,7 @@ mlp_status mlp_tp_forward_residual_dropout(const mlp_bf16* X, const mlp_bf16* A,
 {
     DropoutParams d;
     if (!make_dropout(p, seed, offset, &d)) return MLP_EINVAL;
+    if (T > 0 && !G) return MLP_EINVAL;
     return forward_impl(X, A, a, B, b, R, &d, T, h, f, t, H, G, Z, nullptr, 0, cuda_stream);
 }
 
@@ -460,8 +485,8 @@ mlp_status mlp_tp_dropout_backward(const mlp_bf16* dZ, int T, int h, double p, u
 
 namespace mlp {
 
-// The backward pass. With G == NULL the dH GEMM also recomputes G = GELU(H) into the
-// workspace (after dH) and GEMM 6 reads it from there.
+// The backward pass. With G == NULL (the GELU recompute) GEMM 6 reads H, turning each A tile
+// into G = GELU(H) in shared memory: G is neither kept from the forward nor stored here.
 static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
                                 const mlp_bf16* G, const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX,
                                 mlp_bf16* dA, mlp_bf16* dB, float* da, float* db, void* workspace,
@@ -477,8 +502,7 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     for (const void* p : ptrs)
         if (!aligned16(p)) return MLP_EALIGN;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLP_EALIGN;
-    const size_t need = recompute ? mlp_tp_recompute_workspace_bytes(T, h, f, t) : mlp_tp_workspace_bytes(T, h, f, t);
-    if (workspace_bytes < need) return MLP_EWORKSPACE;
+    if (workspace_bytes < mlp_tp_workspace_bytes(T, h, f, t)) return MLP_EWORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != MLP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -495,23 +519,18 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     const int bn_f = tile_n(fs), bn_h = tile_n(h);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     mlp_bf16* dH = reinterpret_cast<mlp_bf16*>(ws);
-    float* split_ws = reinterpret_cast<float*>(ws + bwd_ws_before_split(T, h, f, recompute));
-    const size_t g_bytes = recompute ? ws_dh_bytes(T, f) : 0;  // the recomputed G follows dH
-    mlp_bf16* Gw = recompute ? reinterpret_cast<mlp_bf16*>(ws + ws_dh_bytes(T, f)) : nullptr;
-    float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + g_bytes);
-    float* dy_part = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + g_bytes + ws_rows_bytes(T, f));
-    const mlp_bf16* Gin = recompute ? Gw : G;
+    float* split_ws = reinterpret_cast<float*>(ws + bwd_ws_before_split(T, h, f));
+    float* dh_rows = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f));
+    float* dy_part = reinterpret_cast<float*>(ws + ws_dh_bytes(T, f) + ws_rows_bytes(T, f));
     const int nsplit = colsum_splits(T);
     CallTimer timer(s);
 
-    // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h. When
-    // recomputing, the same epilogue also writes G = GELU(H).
+    // GEMM 3: dH = (dY*B^T) (.) GELU'(H); B [f,h] is K-major for N = f, K = h.
     GemmArgs g3{};
     if (!map_kmajor(&g3.tmA, dY, h, T, 128) || !map_kmajor(&g3.tmB, B, h, f, kmajor_b_box(T, bn_f)) ||
         !map_store(&g3.tmD0, dH, f, T))
         return MLP_ECUDA;
     g3.tmD1 = g3.tmD0;
-    if (recompute && !map_store(&g3.tmD1, Gw, f, T)) return MLP_ECUDA;
     g3.M = T; g3.N = f; g3.K = h;
     g3.aux = reinterpret_cast<const __nv_bfloat16*>(H);
     g3.ld_aux = f;
@@ -519,9 +538,7 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g3.status = dev->status;
     g3.timeout_ns = kWaitLimitNs;
     const SplitOut so3{split_ws, kSplitWsBytes, dH, nullptr};
-    const cudaError_t e3 = recompute ? gemm<false, false, EPI_DGELU_G>(g3, bn_f, dev->num_sms, s)
-                                     : gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s, &so3);
-    if (e3 != cudaSuccess) return MLP_ECUDA;
+    if (gemm<false, false, EPI_DGELU>(g3, bn_f, dev->num_sms, s, &so3) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DH);
 
     // GEMM 4: dX = sum over shards of dH_i*A_i^T; A [h,f] is K-major for N = h, K = f.
@@ -550,9 +567,10 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     if (gemm<true, true, EPI_PLAIN>(g5, bn_f, dev->num_sms, s, &so5) != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DA);
 
-    // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major.
+    // GEMM 6: dB = G^T*dY (M = f, N = h, K = T), both operands MN-major; recomputing, the A
+    // operand is H and G = GELU(H) is formed on chip.
     GemmArgs g6{};
-    if (!map_mnmajor(&g6.tmA, Gin, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) ||
+    if (!map_mnmajor(&g6.tmA, recompute ? H : G, f, T) || !map_mnmajor(&g6.tmB, dY, h, T) ||
         !map_store(&g6.tmD0, dB, h, f))
         return MLP_ECUDA;
     g6.tmD1 = g6.tmD0;
@@ -560,7 +578,9 @@ static mlp_status backward_impl(const mlp_bf16* X, const mlp_bf16* A, const mlp_
     g6.status = dev->status;
     g6.timeout_ns = kWaitLimitNs;
     const SplitOut so6{split_ws, kSplitWsBytes, dB};
-    if (gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s, &so6) != cudaSuccess) return MLP_ECUDA;
+    const cudaError_t e6 = recompute ? gemm<true, true, EPI_PLAIN_GA>(g6, bn_h, dev->num_sms, s, &so6)
+                                     : gemm<true, true, EPI_PLAIN>(g6, bn_h, dev->num_sms, s, &so6);
+    if (e6 != cudaSuccess) return MLP_ECUDA;
     timer.mark(MLP_K_BWD_DB);
 
     // Bias gradients: db's partial column sums over row slices of dY (da's came out of the
@@ -592,11 +612,7 @@ mlp_status mlp_tp_backward(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16*
     return backward_impl(X, A, B, H, G, dY, T, h, f, t, dX, dA, dB, da, db, workspace, workspace_bytes, cuda_stream);
 }
 
-size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t)
-{
-    if (check_shape(T, h, f, t) != MLP_OK) return 0;
-    return bwd_ws_before_split(T, h, f, true) + split_ws_bytes(T);
-}
+size_t mlp_tp_recompute_workspace_bytes(int T, int h, int f, int t) { return mlp_tp_workspace_bytes(T, h, f, t); }
 
 mlp_status mlp_tp_backward_recompute(const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B, const mlp_bf16* H,
                                      const mlp_bf16* dY, int T, int h, int f, int t, mlp_bf16* dX, mlp_bf16* dA,

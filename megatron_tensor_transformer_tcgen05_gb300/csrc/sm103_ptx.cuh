@@ -20,6 +20,7 @@ enum : int {
     DEV_TIMEOUT_SELFTEST = 6,   // the self-test wait ran out, as it is meant to
     DEV_SMEM_MISALIGNED = 7,    // dynamic shared memory did not start on the 1 KB boundary a kernel
                                 // without alignment slack needs; the kernel did nothing
+    DEV_TIMEOUT_XFORM = 8,      // an operand-transform warp gave up waiting for a loaded A tile
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -57,31 +58,53 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// kCluster: acquire at cluster scope, for a barrier that threads of the peer CTA arrive on
+// after writing shared memory that this CTA's MMAs then read.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Same test, but a thread whose phase is not complete may sleep until it completes (or
 // for up to `hint_ns`) instead of returning at once: waiting costs no issue slots.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
+    if (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
+            : "memory");
     return ok != 0;
 }
 
@@ -91,15 +114,16 @@ constexpr uint32_t kWaitSleepHintNs = 10000000u;  // wakes on completion; the hi
 // *abort is set by another role, or after limit_ns; on a timeout it records `code` in
 // status[0] (first error wins; then status[1..4] = block, thread, where_a, where_b) and
 // raises *abort so that the other roles stop too.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, int* status,
                                                   uint64_t limit_ns, int code,
                                                   int where_a = -1, int where_b = -1)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
+        if (mbar_try_wait_sleep<kCluster>(bar, parity, kWaitSleepHintNs)) return true;
         if ((it & 15u) == 0u) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
@@ -228,6 +252,13 @@ __device__ __forceinline__ void bulk_wait_group()
 __device__ __forceinline__ void prefetch_l2(const void* p)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -38,11 +38,13 @@
 //                  (keep from Philox4x32-10 on the element's index; philox.cuh)
 //   EPI_DGELU      dH = acc * GELU'(H[m,n])                -> stores dH (and, optionally,
 //                  its column sums over each 32-row block in fp32, for the bias gradient)
-//   EPI_DGELU_G    as EPI_DGELU, and G = GELU(H[m,n]) from the same sigmoid -> stores dH, G
 //                  (the backward that recomputes G instead of keeping it from the forward)
 //   EPI_PLAIN      D = acc                                 -> stores D
 //   EPI_SWIGLU     acc = [X A | X Wg] over 128 columns: Ha, Hg, U = SiLU(Ha) Hg -> stores all three
 //   EPI_DSWIGLU    dU = acc: dHa = dU Hg SiLU'(Ha), dHg = dU SiLU(Ha)            -> stores both
+//   EPI_PLAIN_GA, EPI_BIAS_GA   as EPI_PLAIN, EPI_BIAS, with the A operand read as H and
+//                  turned into G = GELU(H) in shared memory by eight operand-transform
+//                  warps before the MMAs read it (the GELU recompute: G never goes to HBM)
 // GELU is the tanh form 0.5 x (1 + tanh u), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated
 // through the identity 1 + tanh u = 2 / (1 + exp(-2u)), which stays accurate where
 // 1 + tanh u is small.
@@ -68,9 +70,13 @@ struct GemmCfg {
     static constexpr int BN_CTA = BN / CG;  // rows of the B operand one CTA loads
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
     static constexpr int EPI = EPI_;
+    // Operand transform: the A tiles hold H and become G = GELU(H) in shared memory before
+    // the MMAs read them; the epilogue is then EPI_B's (plain or + bias).
+    static constexpr bool XFORM = (EPI == EPI_PLAIN_GA || EPI == EPI_BIAS_GA);
+    static constexpr int EPI_B = (EPI == EPI_PLAIN_GA) ? EPI_PLAIN : (EPI == EPI_BIAS_GA) ? EPI_BIAS : EPI;
     // Dual B operand (SwiGLU up-projection): each tile covers OBN = BN/2 output columns,
     // its MMA N = BN spans [A's columns | Wg's columns] of that range.
-    static constexpr bool DUAL = (EPI == EPI_SWIGLU);
+    static constexpr bool DUAL = (EPI_B == EPI_SWIGLU);
     static constexpr int OBN = DUAL ? BN / 2 : BN;
     static constexpr int HALVES = (BN == 512) ? 2 : 1;  // MMAs per k step, each N = MMA_N
     static constexpr int MMA_N = BN / HALVES;
@@ -79,18 +85,20 @@ struct GemmCfg {
     static constexpr int NACC = (BN == 512) ? 1 : 2;
     // epilogues the split-tail fixup can finish: their last tiles may be split
     static constexpr bool SPLITTABLE =
-        (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU);
+        (EPI_B == EPI_PLAIN || EPI_B == EPI_BIAS || EPI_B == EPI_BIAS_GELU || EPI_B == EPI_DGELU);
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int NOUT =
-        (EPI == EPI_SWIGLU) ? 3 : (EPI == EPI_BIAS_GELU || EPI == EPI_DSWIGLU || EPI == EPI_DGELU_G) ? 2 : 1;
+    static constexpr int NOUT = (EPI_B == EPI_SWIGLU) ? 3 : (EPI_B == EPI_BIAS_GELU || EPI_B == EPI_DSWIGLU) ? 2 : 1;
     static constexpr uint32_t STG_BYTES = 32 * 32 * 2;              // one 32x32 bf16 box
     // Epilogue warps: 8 (two per TMEM lane quadrant, taking alternate 32-column chunks) for the
     // one-accumulator 512-wide tiles, whose epilogue holds up the next tile's MMAs until each
     // half is read out; else 4. With 8, each warp stages through one buffer instead of two.
     static constexpr int EPI_WARPS = (NACC == 1) ? 8 : 4;
     static constexpr int EPI_SETS = EPI_WARPS / 4;
+    // Operand-transform warps: 8 GELUs per clock per SM keep pace with a 512-wide tile's MMAs
+    // (one A value per 512 MACs).
+    static constexpr int XF_WARPS = XFORM ? 16 : 0;
     static constexpr int STG_BUFS = EPI_WARPS == 8 ? 1 : 2;
     static constexpr uint32_t EPI_BYTES = EPI_WARPS * STG_BUFS * NOUT * STG_BYTES;
     // Epilogues whose first output is the accumulator (+ bias) rounded to bf16 read each
@@ -98,19 +106,27 @@ struct GemmCfg {
     // before staging and storing anything; the bias + GELU epilogue then computes G from
     // the rounded H.
     static constexpr bool DRAIN_FIRST =
-        NACC == 1 && EPI_WARPS == 8 && (EPI == EPI_PLAIN || EPI == EPI_BIAS || EPI == EPI_BIAS_GELU);
+        NACC == 1 && EPI_WARPS == 8 && !XFORM && (EPI_B == EPI_PLAIN || EPI_B == EPI_BIAS || EPI_B == EPI_BIAS_GELU);
     static constexpr uint32_t TMEM_COLS = NACC * BN;                 // fp32 accumulators
     // 32-column chunks one epilogue warp handles per tile: chunks eset + EPI_SETS * k
     static constexpr int NCH = OBN / 32 / EPI_SETS;
-    static constexpr bool HAS_BIAS = (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_DROPOUT_RES);
-    static constexpr bool DGELU_ANY = (EPI == EPI_DGELU || EPI == EPI_DGELU_G);
+    static constexpr bool HAS_BIAS = (EPI_B == EPI_BIAS || EPI_B == EPI_BIAS_GELU || EPI_B == EPI_BIAS_DROPOUT_RES);
     // as many stages as fit beside the epilogue staging (at most 6 for pairs, 4 alone)
     static constexpr int STAGES_FIT = static_cast<int>((232448u - 1024u - 256u - EPI_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT < ((CG == 2) ? 6 : 4) ? STAGES_FIT : ((CG == 2) ? 6 : 4);
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    // The transform warps work in XF_GROUPS groups; group g owns the ring slots s with
+    // s % XF_GROUPS == g and transforms every fill of them, whole, in order. Fills then move
+    // through several groups at once (each fill's chain of waits, shared-memory round trip
+    // and proxy fence overlaps the others'), and a group never waits on a slot's barrier more
+    // than one phase ahead of its last completed phase.
+    static constexpr int XF_GROUPS = (STAGES % 4 == 0) ? 4 : 2;
+    static constexpr int XF_GROUP_WARPS = XFORM ? XF_WARPS / XF_GROUPS : 1;
+    static_assert(!XFORM || (STAGES % XF_GROUPS == 0 && (A_BYTES / 16) % (32 * XF_GROUP_WARPS) == 0),
+                  "transform groups own whole ring slots and whole 16-byte columns of the A tile");
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + (XFORM ? 2 * STAGES : 0);
     static constexpr uint32_t BAR_BYTES = 8 * NUM_BARS + 16;
     static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA issuer, epilogue
+    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + XF_WARPS);  // producer, MMA issuer, epilogue, transform
     static constexpr uint32_t IDESC = idesc_bf16_f32(BM * CG, MMA_N, A_MN, B_MN);
     static_assert(BN == 128 || BN == 256 || BN == 512, "tile width");
     static_assert(CG == 1 ? BN <= 256 : (BN == 256 || (BN == 512 && !DUAL)), "CTA pairs use 256- or 512-wide tiles");
@@ -370,6 +386,7 @@ template <int BN, bool A_MN, bool B_MN, int EPI, int CG>
 __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) umma_gemm_kernel(const __grid_constant__ GemmArgs args)
 {
     using C = GemmCfg<BN, A_MN, B_MN, EPI, CG>;
+    constexpr int E = C::EPI_B;  // the epilogue (the transform flavours use the plain or bias one)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -377,11 +394,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
     const uint32_t s_stages = base;
     const uint32_t s_epi = base + C::STAGES * C::STAGE_BYTES;
     const uint32_t s_bar = s_epi + C::EPI_BYTES;
-    // barrier map: full[S] | empty[S] | acc_full[2] | acc_empty[2] | drain | tmem slot | abort
+    // barrier map: full[S] | empty[S] | acc_full[2] | acc_empty[2] | drain | (transform
+    // flavours: a_full[S] | xf[S]) | tmem slot | abort. With the transform, each CTA's A tile
+    // lands on its own a_full barrier, its transform warps turn it into G, and xf (in the
+    // pair's even CTA, which issues the MMAs) completes once both CTAs' warps are done.
     const uint32_t b_full = s_bar, b_empty = s_bar + 8u * C::STAGES;
     const uint32_t b_accf = s_bar + 16u * C::STAGES, b_acce = b_accf + 16u;
     const uint32_t b_drain = b_acce + 16u;
-    const uint32_t s_slot = b_drain + 8u;
+    const uint32_t b_afull = b_drain + 8u, b_xf = b_afull + 8u * C::STAGES;
+    const uint32_t s_slot = b_drain + 8u + (C::XFORM ? 16u * C::STAGES : 0u);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (s_slot - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (s_slot + 4u - base));
 
@@ -419,6 +440,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             mbar_init(b_acce + 8u * a, C::EPI_WARPS * CG);  // one arrive per epilogue warp of the pair
         }
         mbar_init(b_drain, 1);
+        if (C::XFORM)
+            for (int s = 0; s < C::STAGES; ++s) {
+                mbar_init(b_afull + 8u * s, 1);
+                mbar_init(b_xf + 8u * s, C::XF_GROUP_WARPS * CG);  // one transform group, in each CTA of the pair
+            }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&args.tmA);
@@ -473,13 +499,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     const int k0 = (seg2 ? kb - args.kb_split : kb) * C::BK;
                     const CUtensorMap* tA = seg2 ? &args.tmA2 : &args.tmA;
                     const CUtensorMap* tB = seg2 ? &args.tmB2 : &args.tmB;
+                    // transform flavours: this CTA's A tile lands on its own a_full barrier
+                    const uint32_t fa = C::XFORM ? b_afull + 8u * stage : fb;
                     if (CG == 1) {
-                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        if (C::XFORM) mbar_arrive_expect_tx(fa, C::A_BYTES);
+                        mbar_arrive_expect_tx(fb, C::XFORM ? C::B_BYTES : C::STAGE_BYTES);
                         if (A_MN) {
-                            tma_load_2d(sa, tA, m_cta, k0, fb);
-                            tma_load_2d(sa + 8192u, tA, m_cta + 64, k0, fb);
+                            tma_load_2d(sa, tA, m_cta, k0, fa);
+                            tma_load_2d(sa + 8192u, tA, m_cta + 64, k0, fa);
                         } else {
-                            tma_load_2d(sa, tA, k0, m_cta, fb);
+                            tma_load_2d(sa, tA, k0, m_cta, fa);
                         }
                         if (C::DUAL) {  // rows [0, BN/2): A's columns; [BN/2, BN): Wg's, same range
 #pragma unroll
@@ -498,8 +527,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         // CTA alone arms with the pair's total (with two pairs, the B half the
                         // other pair multicasts into this pair completes there too).
                         const uint32_t fb0 = mapa_shared(fb, lead);
-                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
-                        if (A_MN) {
+                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (C::XFORM ? C::B_BYTES : C::STAGE_BYTES));
+                        if (C::XFORM) {
+                            mbar_arrive_expect_tx(fa, C::A_BYTES);
+                            if (A_MN) {
+                                tma_load_2d(sa, tA, m_cta, k0, fa);
+                                tma_load_2d(sa + 8192u, tA, m_cta + 64, k0, fa);
+                            } else {
+                                tma_load_2d(sa, tA, k0, m_cta, fa);
+                            }
+                        } else if (A_MN) {
                             tma_load_2d_pair(sa, tA, m_cta, k0, fb0);
                             tma_load_2d_pair(sa + 8192u, tA, m_cta + 64, k0, fb0);
                         } else {
@@ -545,6 +582,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             }
             if (!ok) {
                 // Let every copy this CTA started land before the CTA may exit.
+                if (C::XFORM) {  // its A tiles, on its own barriers
+                    volatile int never = 0;
+                    for (int s = 0; s < C::STAGES; ++s)
+                        if (issued & (1u << s))
+                            mbar_wait_bounded(b_afull + 8u * s, (par >> s) & 1u, &never, args.status, kDrainLimitNs,
+                                              DEV_TIMEOUT_DRAIN);
+                }
                 if (rank == 0) {
                     volatile int never = 0;
                     for (int s = 0; s < C::STAGES; ++s)
@@ -576,7 +620,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 bool half1_free = C::NACC == 2;
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(b_full + 8u * stage, phase, abort_flag, args.status, limit,
-                                           DEV_TIMEOUT_MMA_FULL, tile, kb)) {
+                                           DEV_TIMEOUT_MMA_FULL, tile, kb) ||
+                        (C::XFORM && !mbar_wait_bounded<CG == 2>(b_xf + 8u * stage, phase, abort_flag, args.status,
+                                                                 limit, DEV_TIMEOUT_MMA_FULL, tile, kb))) {
                         ok = false;
                         break;
                     }
@@ -652,6 +698,53 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 mbar_wait_bounded(b_drain, 0, &never, args.status, kDrainLimitNs, DEV_TIMEOUT_DRAIN);
             }
         }
+    } else if (C::XFORM && warp >= 2 + C::EPI_WARPS) {
+        // --------------------------- operand transform ----------------------------
+        // Each landed A tile of H (16 KB: 128 rows x 64 k) becomes G = GELU(H) in place, 16
+        // bytes (8 values) per thread and step, with the same arithmetic as the forward's
+        // bias + GELU epilogue (gelu_bf16x2), so G matches the stored G bit for bit. The
+        // values are elementwise, so the tile's layout (K- or MN-major, swizzled) does not
+        // matter; zero fill past the matrix edges stays zero (GELU(0) = 0).
+        const int xw = warp - (2 + C::EPI_WARPS);
+        const int group = xw / C::XF_GROUP_WARPS;
+        const int xt = 32 * (xw % C::XF_GROUP_WARPS) + lane;  // thread within its group
+        const uint32_t xf0 = (CG == 2) ? mapa_shared(b_xf, lead) : b_xf;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int u = unit; ok && u < num_work; u += num_units) {
+            int tile, kb_lo, kb_hi, part;
+            work_unit(u, n_whole, split_k, num_kb, tile, kb_lo, kb_hi, part);
+            for (int kb = kb_lo; kb < kb_hi; ++kb) {
+                const uint32_t st = stage, ph = phase;
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (static_cast<int>(st) % C::XF_GROUPS != group) continue;  // another group's ring slot
+                // every lane waits, as each reads bytes the copy wrote; the warp acts on all
+                const bool got = mbar_wait_bounded(b_afull + 8u * st, ph, abort_flag, args.status, limit,
+                                                   DEV_TIMEOUT_XFORM, tile, kb);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = s_stages + st * C::STAGE_BYTES;
+#pragma unroll 4
+                for (int i = 0; i < static_cast<int>(C::A_BYTES / 16) / (32 * C::XF_GROUP_WARPS); ++i) {
+                    const uint32_t ad = sa + 16u * static_cast<uint32_t>(xt + 32 * C::XF_GROUP_WARPS * i);
+                    const uint4 hv = lds_v4(ad);
+                    sts_v4(ad, gelu_bf16x2(hv.x), gelu_bf16x2(hv.y), gelu_bf16x2(hv.z), gelu_bf16x2(hv.w));
+                }
+                fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 2)
+                        mbar_arrive_cluster(xf0 + 8u * st);
+                    else
+                        mbar_arrive(b_xf + 8u * st);
+                }
+            }
+        }
     } else {
         // ------------------------------ epilogue ----------------------------------
         const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the ones this warp may read
@@ -675,7 +768,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 const int n = n0 + 32 * (eset + C::EPI_SETS * wc) + 8 * (lane & 3);
                 if (wc < C::NCH && n < N) bias_w = ldg_nc_v4(args.bias + n);
             }
-            if (C::DGELU_ANY && part < 0 && row < M) {
+            if (E == EPI_DGELU && part < 0 && row < M) {
 #pragma unroll
                 for (int k = 0; k < 3; ++k) {
                     const int n = n0 + 32 * (eset + C::EPI_SETS * k);
@@ -702,13 +795,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             // hnext: the aux row segment of this warp's next chunk (H, the residual, Ha);
             // gnext: Hg.
             uint4 hnext[4], gnext[4];
-            if (EPI == EPI_DGELU || EPI == EPI_DGELU_G || EPI == EPI_BIAS_DROPOUT_RES || EPI == EPI_DSWIGLU) {
+            if (E == EPI_DGELU || E == EPI_BIAS_DROPOUT_RES || E == EPI_DSWIGLU) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int n = n0 + 32 * eset + 8 * i;
                     const bool in = row < M && n < N;
                     hnext[i] = in ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n) : make_uint4(0, 0, 0, 0);
-                    if (EPI == EPI_DSWIGLU)
+                    if (E == EPI_DSWIGLU)
                         gnext[i] = in ? ldg_nc_v4(args.aux2 + static_cast<size_t>(row) * args.ld_aux + n)
                                       : make_uint4(0, 0, 0, 0);
                 }
@@ -730,7 +823,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                        if (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) add_bias_chunk(v, bias_w, hh * KPH + k);
+                        if (E == EPI_BIAS || E == EPI_BIAS_GELU) add_bias_chunk(v, bias_w, hh * KPH + k);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) pk[k][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                     }
@@ -748,7 +841,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         const int nc = n0 + 32 * c;
                         if (nc >= N || row_blk >= M) continue;
                         uint32_t p1[16];
-                        if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H
+                        if (E == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H
 #pragma unroll
                             for (int j = 0; j < 16; ++j) p1[j] = gelu_bf16x2(pk[k][j]);
                         }
@@ -810,7 +903,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 uint32_t p0[16], p1[16], p2[16];
-                if (EPI == EPI_SWIGLU) {  // v = Ha = X A, r2 = Hg = X Wg: keep both, U = SiLU(Ha) Hg
+                if (E == EPI_SWIGLU) {  // v = Ha = X A, r2 = Hg = X Wg: keep both, U = SiLU(Ha) Hg
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float ga = __uint_as_float(r2[2 * j]), gb = __uint_as_float(r2[2 * j + 1]);
@@ -818,7 +911,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         p2[j] = pack_bf16x2(silu_f(v[2 * j]) * ga, silu_f(v[2 * j + 1]) * gb);
                     }
                 }
-                if (EPI == EPI_DSWIGLU) {  // v = dU; dHa = dU Hg SiLU'(Ha) (in v), dHg = dU SiLU(Ha)
+                if (E == EPI_DSWIGLU) {  // v = dU; dHa = dU Hg SiLU'(Ha) (in v), dHg = dU SiLU(Ha)
                     float ha[32], hg[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -844,7 +937,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     }
                 }
                 if (C::HAS_BIAS) add_bias_chunk(v, bias_w, wc);
-                if (EPI == EPI_BIAS_DROPOUT_RES) {
+                if (E == EPI_BIAS_DROPOUT_RES) {
                     float rv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], rv + 8 * i);
@@ -868,7 +961,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     }
                 }
                 float cs0 = 0.0f;  // GELU' epilogues: column sum of this warp's 32 rows, column nc + lane
-                if (EPI == EPI_DGELU || EPI == EPI_DGELU_G) {
+                if (E == EPI_DGELU) {
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
@@ -887,11 +980,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     for (int j = 0; j < 16; ++j) {  // dH = dG GELU'(H), two columns at a time
                         const GeluPair gp = gelu_sigmoid_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
                         f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), gelu_grad_pair(gp)), v[2 * j], v[2 * j + 1]);
-                        if (EPI == EPI_DGELU_G) {  // and G = GELU(H) from the same sigmoid
-                            float g0, g1;
-                            f2_unpack(gelu_value_pair(gp), g0, g1);
-                            p1[j] = pack_bf16x2(g0, g1);
-                        }
                     }
                     if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
                         float cs[32];
@@ -903,7 +991,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                if (EPI == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H, as in every path
+                if (E == EPI_BIAS_GELU) {  // G = GELU(H) of the rounded H, as in every path
 #pragma unroll
                     for (int j = 0; j < 16; ++j) p1[j] = gelu_bf16x2(p0[j]);
                 }
@@ -924,7 +1012,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
                 if (C::STG_BUFS == 2) sel ^= 1u;
                 // the column sums go out after the staging fence and the store
-                if ((EPI == EPI_DGELU || EPI == EPI_DGELU_G) && args.colsum_rows && nc + lane < N)
+                if (E == EPI_DGELU && args.colsum_rows && nc + lane < N)
                     args.colsum_rows[static_cast<size_t>(row_blk >> 5) * N + nc + lane] = cs0;
             }
             if (C::NACC == 2) {

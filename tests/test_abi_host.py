@@ -43,7 +43,7 @@ def test_forward_workspace_bytes():
     assert fw == 40 * 1024 * 1024  # one 256 KB part per SM of up to 160 SMs
     # every backward workspace holds the split-tail region after its own intermediates
     assert _lib.mlp_tp_workspace_bytes(128, 64, 256, 2) >= 128 * 256 * 2 + fw
-    assert _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 2) >= 2 * 128 * 256 * 2 + fw
+    assert _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 2) == _lib.mlp_tp_workspace_bytes(128, 64, 256, 2)
     assert _lib.mlp_tp_swiglu_workspace_bytes(128, 64, 256, 2) >= 2 * 128 * 256 * 2 + fw
 
 
@@ -134,9 +134,27 @@ def test_attention_rejects_null_misaligned_and_short_workspace(L):
 
 def test_recompute_backward_workspace_and_checks(L):
     need = _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 2)
-    assert need >= _lib.mlp_tp_workspace_bytes(128, 64, 256, 2) + 128 * 256 * 2  # plus the recomputed G
+    assert need == _lib.mlp_tp_workspace_bytes(128, 64, 256, 2)  # G is never stored, not even here
     assert _lib.mlp_tp_recompute_workspace_bytes(128, 64, 256, 3) == 0
     args = [FAKE] * 5 + [128, 64, 256, 2] + [FAKE] * 5
     assert L.mlp_tp_backward_recompute(*args, FAKE, need - 256, None) == _lib.STATUS_CODES["MLP_EWORKSPACE"]
     bad = [FAKE] * 5 + [128, 64, 256, 3] + [FAKE] * 5
     assert L.mlp_tp_backward_recompute(*bad, FAKE, need, None) == _lib.STATUS_CODES["MLP_ESHAPE"]
+
+
+def test_recompute_forward_checks(L):
+    """The forward that keeps H alone: argument checks before any launch (no G argument)."""
+    n0 = _lib.mlp_tp_launch_count()
+    ok = [FAKE] * 5 + [128, 64, 256, 2] + [FAKE] * 2
+    assert L.mlp_tp_forward_recompute(*([FAKE] * 5), 128, 64, 256, 3, FAKE, FAKE, None, 0, None) == \
+        _lib.STATUS_CODES["MLP_ESHAPE"]
+    assert L.mlp_tp_forward_recompute(*([FAKE] * 5), 128, 64, 256, 2, None, FAKE, None, 0, None) == \
+        _lib.STATUS_CODES["MLP_EINVAL"]
+    assert L.mlp_tp_forward_recompute(*ok, FAKE + 8, 1 << 20, None) == _lib.STATUS_CODES["MLP_EALIGN"]
+    assert L.mlp_tp_forward_recompute(*([FAKE] * 4), FAKE + 2, 128, 64, 256, 2, FAKE, FAKE, None, 0, None) == \
+        _lib.STATUS_CODES["MLP_EALIGN"]
+    # mlp_tp_forward still needs its G
+    assert L.mlp_tp_forward(*([FAKE] * 5), 128, 64, 256, 2, FAKE, None, FAKE, None, 0, None) == \
+        _lib.STATUS_CODES["MLP_EINVAL"]
+    assert _lib.mlp_tp_launch_count() == n0
+

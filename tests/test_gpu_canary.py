@@ -7,8 +7,8 @@ pattern, and every input must be bit-for-bit unchanged. The shapes reach every h
 store of the library on ragged sizes and every branch of the GEMM launch planner: the split
 tails' fp32 parts and their fixup (splitk_fixup_kernel), the dH epilogue's per-32-row column
 sums (in the workspace) and the column-sum kernels (da, db), the attention block's L and D
-(D in the workspace), the dropout backward, the SwiGLU epilogues, the GELU-recompute
-backward, and the allocation-free bias-gradient entry point. A one-element overrun past the
+(D in the workspace), the dropout backward, the SwiGLU epilogues, the GELU recompute's
+forward and backward, and the allocation-free bias-gradient entry point. A one-element overrun past the
 end of any output, or a write before its start, changes a guard byte and fails the test."""
 import numpy as np
 import pytest
@@ -106,11 +106,14 @@ def test_mlp_forward_backward_stay_in_bounds(T, h, f, t):
 
 
 @pytest.mark.parametrize("T,h,f,t", MLP_SHAPES[::3], ids=[f"T{T}-h{h}-f{f}-t{t}" for T, h, f, t in MLP_SHAPES[::3]])
-def test_recompute_backward_stays_in_bounds(T, h, f, t):
+def test_recompute_forward_backward_stay_in_bounds(T, h, f, t):
+    """The GELU recompute: H-only forward and the backward from H (A operands transformed on chip)."""
     inp = {k: v.cuda() for k, v in make_inputs(T, h, f, seed=T + h, sdy=1.0).items()}
     o = _mlp_outs(T, h, f, t, recompute=True)
+    del o["G"]
     g = {k: v.t for k, v in o.items()}
-    _lib.mlp_tp_forward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], T, h, f, t, g["H"], g["G"], g["Y"], None, 0)
+    _run_and_check(o, inp, lambda: _lib.mlp_tp_forward_recompute(
+        inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], T, h, f, t, g["H"], g["Y"], g["fws"], g["fws"].numel()))
     H = g["H"].clone()
     _run_and_check(o, dict(inp, H=H), lambda: _lib.mlp_tp_backward_recompute(
         inp["X"], inp["A"], inp["B"], H, inp["dY"], T, h, f, t, g["dX"], g["dA"], g["dB"], g["da"], g["db"], g["ws"],

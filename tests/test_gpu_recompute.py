@@ -1,5 +1,8 @@
-"""GPU parity of the backward that recomputes G = GELU(H) instead of keeping the forward's G."""
-import numpy as np
+"""GPU parity of the GELU recompute, in which G = GELU(H) is never stored: the forward keeps H
+alone and its down-projection reads H, turning each A tile into G in shared memory; the
+backward's dB GEMM does the same. G there is the forward epilogue's G bit for bit, so the
+forward's Y and every gradient must equal those of the path that keeps G, bit for bit, and
+match the fp64 oracle."""
 import pytest
 import torch
 
@@ -20,36 +23,68 @@ def _built():
     _lib.lib()
 
 
-@pytest.mark.parametrize("T,h,f,t", [(128, 64, 256, 2), (300, 200, 800, 2), (512, 512, 2048, 4), (777, 264, 1536, 3),
-                                     (2560, 512, 4096, 8)])
-def test_backward_with_gelu_recompute(T, h, f, t):
+# one CTA per tile; ragged pairs; 256-wide pairs; odd shard counts; 512-wide tiles on clusters of
+# two CTA pairs for the down-projection (N = h, K = f) and dB (N = h, K = T); split tails
+SHAPES = [(128, 64, 256, 2), (300, 200, 800, 2), (512, 512, 2048, 4), (777, 264, 1536, 3), (2560, 512, 4096, 8),
+          (2048, 1024, 4096, 2), (512, 1024, 4096, 2), (2048, 256, 1024, 2)]
+
+
+@pytest.mark.parametrize("T,h,f,t", SHAPES, ids=[f"T{T}-h{h}-f{f}-t{t}" for T, h, f, t in SHAPES])
+def test_recompute_forward_and_backward(T, h, f, t):
     inp = make_inputs(T, h, f, seed=3, sdy=1.0)
     dev = {k: v.cuda() for k, v in inp.items()}
     buf = block.empty_buffers(T, h, f, t)
-    block.forward(dev, buf, t)
-    block.backward(dev, buf, t)  # the reference: the backward that reads the forward's G
-    kept = {k: buf[k].clone() for k in ("dX", "dA", "dB", "da", "db")}
-    G_fwd = buf["G"].clone()
-    buf["G"].fill_(float("nan"))  # the forward's G was scratch: the recompute must not read it
+    block.step(dev, buf, t)  # the reference: the path that keeps G
+    kept = {k: buf[k].clone() for k in ("H", "Y", "dX", "dA", "dB", "da", "db")}
+    fws = torch.empty((_lib.mlp_tp_forward_workspace_bytes(),), dtype=torch.uint8, device="cuda")
+
+    H = torch.full((T, f), float("nan"), dtype=torch.bfloat16, device="cuda")
+    Y = torch.full((T, h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _lib.mlp_tp_forward_recompute(dev["X"], dev["A"], dev["a"], dev["B"], dev["b"], T, h, f, t, H, Y, fws,
+                                  fws.numel())
+    assert _lib.mlp_tp_query_device_status() == 0, _lib.mlp_tp_last_device_where()
+    assert torch.equal(H, kept["H"]), "H differs from the forward that keeps G"
+    assert torch.equal(Y, kept["Y"]), "Y differs from the forward that keeps G"
+
     ws_bytes = _lib.mlp_tp_recompute_workspace_bytes(T, h, f, t)
     ws = torch.empty((ws_bytes,), dtype=torch.uint8, device="cuda")
-    out = {k: torch.full_like(v, float("nan")) for k, v in kept.items()}
-    _lib.mlp_tp_backward_recompute(dev["X"], dev["A"], dev["B"], buf["H"], dev["dY"], T, h, f, t, out["dX"],
-                                   out["dA"], out["dB"], out["da"], out["db"], ws, ws_bytes)
-    assert _lib.mlp_tp_query_device_status() == 0
-    for k in ("dX", "dA", "da", "db"):  # these never touch G: bitwise the kept-G backward
-        assert torch.equal(out[k], kept[k]), k
-    # the forward computes G from the rounded H, as the recompute must: the same G to the bit,
-    # hence the same dB
-    G_rec = ws[((T * f * 2 + 255) // 256) * 256:][: T * f * 2].view(torch.bfloat16).view(T, f)
-    assert torch.equal(G_rec, G_fwd)
-    assert torch.equal(out["dB"], kept["dB"])
-    ref = oracle.fwd_bwd({k: v.double().numpy() for k, v in inp.items()})
-    assert_close("dB", out["dB"], ref["dB"])
-    assert_close("G recomputed", G_rec, ref["G"])
+    out = {k: torch.full_like(kept[k], float("nan")) for k in ("dX", "dA", "dB", "da", "db")}
+    _lib.mlp_tp_backward_recompute(dev["X"], dev["A"], dev["B"], H, dev["dY"], T, h, f, t, out["dX"], out["dA"],
+                                   out["dB"], out["da"], out["db"], ws, ws_bytes)
+    assert _lib.mlp_tp_query_device_status() == 0, _lib.mlp_tp_last_device_where()
+    for k in ("dX", "dA", "dB", "da", "db"):
+        assert torch.equal(out[k], kept[k]), f"{k} differs from the backward that keeps G"
+
+    ref = oracle.fwd_bwd(inp)
+    for k, v in (("H", H), ("Y", Y), ("dB", out["dB"]), ("dX", out["dX"]), ("da", out["da"])):
+        assert_close(k, v, ref[k])
     fs = f // t
     for i in range(t):
         assert_close(f"dB shard {i}", out["dB"][i * fs:(i + 1) * fs], ref["dB"][i * fs:(i + 1) * fs])
+
+
+def test_recompute_is_deterministic():
+    T, h, f, t = 2048, 1024, 4096, 2
+    inp = make_inputs(T, h, f, seed=9, sdy=1.0)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    ws_bytes = _lib.mlp_tp_recompute_workspace_bytes(T, h, f, t)
+    runs = []
+    for _ in range(2):
+        H = torch.empty((T, f), dtype=torch.bfloat16, device="cuda")
+        Y = torch.empty((T, h), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty((ws_bytes,), dtype=torch.uint8, device="cuda")
+        g = {"dX": torch.empty((T, h), dtype=torch.bfloat16, device="cuda"),
+             "dA": torch.empty((h, f), dtype=torch.bfloat16, device="cuda"),
+             "dB": torch.empty((f, h), dtype=torch.bfloat16, device="cuda"),
+             "da": torch.empty((f,), device="cuda"), "db": torch.empty((h,), device="cuda")}
+        _lib.mlp_tp_forward_recompute(dev["X"], dev["A"], dev["a"], dev["B"], dev["b"], T, h, f, t, H, Y, ws,
+                                      ws_bytes)
+        _lib.mlp_tp_backward_recompute(dev["X"], dev["A"], dev["B"], H, dev["dY"], T, h, f, t, g["dX"], g["dA"],
+                                       g["dB"], g["da"], g["db"], ws, ws_bytes)
+        assert _lib.mlp_tp_query_device_status() == 0
+        runs.append(dict(g, Y=Y))
+    for k in runs[0]:
+        assert torch.equal(runs[0][k], runs[1][k]), k
 
 
 def test_recompute_rejects_short_workspace():
@@ -58,7 +93,7 @@ def test_recompute_rejects_short_workspace():
     dev = {k: v.cuda() for k, v in inp.items()}
     buf = block.empty_buffers(T, h, f, t)
     need = _lib.mlp_tp_recompute_workspace_bytes(T, h, f, t)
-    assert need > _lib.mlp_tp_workspace_bytes(T, h, f, t)
+    assert need == _lib.mlp_tp_workspace_bytes(T, h, f, t)
     ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
     with pytest.raises(_lib.MlpError) as ei:
         _lib.mlp_tp_backward_recompute(dev["X"], dev["A"], dev["B"], buf["H"], dev["dY"], T, h, f, t, buf["dX"],
