@@ -182,8 +182,12 @@ __device__ __forceinline__ float ex2_approx(float z)
 // reciprocal 1 / (1 + e) runs on the FMA pipe: Newton's iteration r <- r + r (1 - d r) from
 // the integer estimate bits(r0) = R - bits(d), R = 0x7EF311C0 (chosen by search over all
 // mantissas: |r0 d - 1| <= 5.06% for every normal d); three steps leave <= 1 ulp. Since
-// 1 - s = e s, s (1 - s) = s^2 e has no cancellation. z is capped at 120 (s < 1e-36 there),
-// so d and r0 stay normal numbers.
+// 1 - s = e s, s (1 - s) = s^2 e has no cancellation.
+// x is first raised to at least -kGeluFloor (z <= 117.9 there, so e, d and r0 stay normal
+// numbers): below it GELU(x) and GELU'(x) are below 3.1e-35 in magnitude, which is what the
+// clamped x gives, and a huge negative x can no longer meet a tiny s in x s. GELU' also caps
+// x at +kGeluFloor (GELU' = 1 in fp32 from there on), so that x^2 stays finite where e = 0.
+constexpr float kGeluFloor = 9.75f;
 struct GeluPair {
     f32x2_t x, x2, e, s;
 };
@@ -193,11 +197,13 @@ __device__ __forceinline__ GeluPair gelu_sigmoid_pair(f32x2_t x)
     constexpr float kC0 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654);
     constexpr float kC1 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
     GeluPair g;
-    g.x = x;
-    g.x2 = f2_mul(x, x);
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    g.x = f2_pack(fmaxf(x0, -kGeluFloor), fmaxf(x1, -kGeluFloor));
+    g.x2 = f2_mul(g.x, g.x);
     float z0, z1;
-    f2_unpack(f2_mul(x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
-    g.e = f2_pack(ex2_approx(fminf(z0, 120.0f)), ex2_approx(fminf(z1, 120.0f)));
+    f2_unpack(f2_mul(g.x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
+    g.e = f2_pack(ex2_approx(z0), ex2_approx(z1));
     const f32x2_t nd = f2_fma(g.e, f2_splat(-1.0f), f2_splat(-1.0f));  // -(1 + e)
     float d0, d1;
     f2_unpack(nd, d0, d1);
@@ -222,6 +228,36 @@ __device__ __forceinline__ f32x2_t gelu_grad_pair(const GeluPair& g)
     return f2_fma(q, w, g.s);
 }
 
+__device__ __forceinline__ float rcp_approx_f(float d)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
+// GELU'(x) for the dH epilogue, which is bound by its instruction count, not by the
+// special-function pipe: the same e and formula, with s = 1 / (1 + e) from the hardware's
+// approximate reciprocal (one special-function op, <= 1 ulp) in place of the seed and three
+// Newton steps (eight FMA-pipe instructions a pair). G itself keeps the Newton form, whose
+// bits the GELU recompute's operand transform must reproduce without loading the
+// special-function pipe twice per value.
+__device__ __forceinline__ f32x2_t gelu_grad_fast_pair(f32x2_t x)
+{
+    constexpr float kC0 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654);
+    constexpr float kC1 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
+    GeluPair g;
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    g.x = f2_pack(fminf(fmaxf(x0, -kGeluFloor), kGeluFloor), fminf(fmaxf(x1, -kGeluFloor), kGeluFloor));
+    g.x2 = f2_mul(g.x, g.x);
+    float z0, z1;
+    f2_unpack(f2_mul(g.x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
+    const float e0 = ex2_approx(z0), e1 = ex2_approx(z1);
+    g.e = f2_pack(e0, e1);
+    g.s = f2_pack(rcp_approx_f(1.0f + e0), rcp_approx_f(1.0f + e1));
+    return gelu_grad_pair(g);
+}
+
 // Scalar forms (the split-tail fixup): the pair code on (x, x), so every path gets the same bits.
 __device__ __forceinline__ float gelu_tanh_f(float x)
 {
@@ -232,7 +268,7 @@ __device__ __forceinline__ float gelu_tanh_f(float x)
 __device__ __forceinline__ float gelu_tanh_grad_f(float x)
 {
     float lo, hi;
-    f2_unpack(gelu_grad_pair(gelu_sigmoid_pair(f2_pack(x, x))), lo, hi);
+    f2_unpack(gelu_grad_fast_pair(f2_pack(x, x)), lo, hi);
     return lo;
 }
 
@@ -978,8 +1014,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         prefetch_l2(args.aux + static_cast<size_t>(row) * args.ld_aux + nc + 96 * C::EPI_SETS);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {  // dH = dG GELU'(H), two columns at a time
-                        const GeluPair gp = gelu_sigmoid_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
-                        f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), gelu_grad_pair(gp)), v[2 * j], v[2 * j + 1]);
+                        const f32x2_t gd = gelu_grad_fast_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
+                        f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), gd), v[2 * j], v[2 * j + 1]);
                     }
                     if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
                         float cs[32];
