@@ -110,6 +110,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 constexpr uint32_t kWaitSleepHintNs = 10000000u;  // wakes on completion; the hint only caps the nap
 
+// Non-blocking test of the phase with the given parity: never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Gives up (returns false) when
 // *abort is set by another role, or after limit_ns; on a timeout it records `code` in
 // status[0] (first error wins; then status[1..4] = block, thread, where_a, where_b) and

@@ -651,9 +651,59 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                // one accumulator: half 1 may still be draining; its release is awaited just
-                // before the first MMA that writes it (after the first k block's half 0)
+                // One accumulator: half 1 may still be draining when the tile starts. Until the
+                // epilogue releases it, each k block's half-0 MMAs are issued and its stage is
+                // held with its half-1 MMAs deferred (at most STAGES - 1 stages, so the producer
+                // never waits on a stage this loop needs next); once half 1 is free the deferred
+                // half-1 MMAs go out in k order, so each half accumulates in the same order as
+                // without deferral and the results are the same bits.
                 bool half1_free = C::NACC == 2;
+                int ndef = 0, def_kb = 0;  // deferred k blocks: def_kb, def_kb + 1, ...
+                uint32_t def_stage = 0;    // the first one's stage
+                auto issue_half = [&](uint32_t st, int kbi, int h) {
+                    const uint32_t sa = s_stages + st * C::STAGE_BYTES;
+                    const uint32_t sbh = sa + C::A_BYTES + 16384u * h;
+#pragma unroll
+                    for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
+                        // K-major: next 16 elements are 32 bytes further along the swizzled
+                        // row. MN-major: next 16 k-rows are two 8-row (1024-byte) groups on.
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                                 : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sbh + 2048u * k, 8192u, 1024u)
+                                                 : smem_desc_sw128(sbh + 32u * k, 16u, 1024u);
+                        const uint32_t accum = (kbi != kb_lo || k != 0) ? 1u : 0u;
+                        if (CG == 2)
+                            umma_bf16_pair(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
+                        else
+                            umma_bf16(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
+                    }
+                };
+                // the stage is free, in both CTAs (and, with two pairs, in the other pair's,
+                // which multicast into it), once the MMAs issued so far finish
+                auto release = [&](uint32_t st) {
+                    if (CG == 2) {
+                        umma_commit_pair_both(b_empty + 8u * st, lead + 1u);
+                        if (npc == 2) {
+                            const uint32_t other = lead ^ 2u;
+                            umma_commit_pair(mapa_shared(b_empty + 8u * st, other));
+                            umma_commit_pair(mapa_shared(b_empty + 8u * st, other + 1u));
+                        }
+                    } else {
+                        umma_commit(b_empty + 8u * st);
+                    }
+                };
+                // half 1 released: the deferred k blocks' half-1 MMAs, then their stages
+                auto flush = [&]() {
+                    tc_fence_after();
+                    half1_free = true;
+                    uint32_t st = def_stage;
+                    for (int i = 0; i < ndef; ++i) {
+                        issue_half(st, def_kb + i, 1);
+                        release(st);
+                        if (++st == C::STAGES) st = 0;
+                    }
+                    ndef = 0;
+                };
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait_bounded(b_full + 8u * stage, phase, abort_flag, args.status, limit,
                                            DEV_TIMEOUT_MMA_FULL, tile, kb) ||
@@ -663,53 +713,48 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = s_stages + stage * C::STAGE_BYTES;
-                    const uint32_t sb = sa + C::A_BYTES;
-#pragma unroll
-                    for (int h = 0; h < C::HALVES; ++h) {
-                        if (h == 1 && !half1_free) {
-                            if (!mbar_wait_bounded(b_acce + 8u, acc_phase ^ 1u, abort_flag, args.status, limit,
-                                                   DEV_TIMEOUT_MMA_ACC, tile, -2)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            half1_free = true;
-                        }
-#pragma unroll
-                        for (int k = 0; k < C::BK / C::UMMA_K; ++k) {
-                            // K-major: next 16 elements are 32 bytes further along the swizzled
-                            // row. MN-major: next 16 k-rows are two 8-row (1024-byte) groups on.
-                            const uint32_t sbh = sb + 16384u * h;
-                            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                                     : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-                            const uint64_t bd = B_MN ? smem_desc_sw128(sbh + 2048u * k, 8192u, 1024u)
-                                                     : smem_desc_sw128(sbh + 32u * k, 16u, 1024u);
-                            const uint32_t accum = (kb != kb_lo || k != 0) ? 1u : 0u;
-                            if (CG == 2)
-                                umma_bf16_pair(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
-                            else
-                                umma_bf16(d_tmem + C::MMA_N * h, ad, bd, C::IDESC, accum);
-                        }
-                    }
-                    if (!ok) break;
                     any = true;
-                    // the stage is free, in both CTAs (and, with two pairs, in the other pair's,
-                    // which multicast into it), once these MMAs finish
-                    if (CG == 2) {
-                        umma_commit_pair_both(b_empty + 8u * stage, lead + 1u);
-                        if (npc == 2) {
-                            const uint32_t other = lead ^ 2u;
-                            umma_commit_pair(mapa_shared(b_empty + 8u * stage, other));
-                            umma_commit_pair(mapa_shared(b_empty + 8u * stage, other + 1u));
+                    issue_half(stage, kb, 0);
+                    if (C::HALVES == 2) {
+                        if (!half1_free) {
+                            bool freed = mbar_test_wait(b_acce + 8u, acc_phase ^ 1u);
+                            if (!freed && ndef + 1 >= C::STAGES) {  // no stage left to hold: wait
+                                if (!mbar_wait_bounded(b_acce + 8u, acc_phase ^ 1u, abort_flag, args.status, limit,
+                                                       DEV_TIMEOUT_MMA_ACC, tile, -2)) {
+                                    ok = false;
+                                    break;
+                                }
+                                freed = true;
+                            }
+                            if (freed) {
+                                flush();
+                            } else {  // hold this stage; its half 1 comes later
+                                if (ndef == 0) {
+                                    def_stage = stage;
+                                    def_kb = kb;
+                                }
+                                ++ndef;
+                                if (++stage == C::STAGES) {
+                                    stage = 0;
+                                    phase ^= 1u;
+                                }
+                                continue;
+                            }
                         }
-                    } else {
-                        umma_commit(b_empty + 8u * stage);
+                        issue_half(stage, kb, 1);
                     }
+                    release(stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+                if (ok && ndef > 0) {  // the tile's k blocks ran out before half 1 was released
+                    if (!mbar_wait_bounded(b_acce + 8u, acc_phase ^ 1u, abort_flag, args.status, limit,
+                                           DEV_TIMEOUT_MMA_ACC, tile, -2))
+                        ok = false;
+                    else
+                        flush();
                 }
                 if (!ok) break;
                 // accumulator ready for the epilogue warps of both CTAs
