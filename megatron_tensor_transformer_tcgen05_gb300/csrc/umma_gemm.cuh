@@ -856,6 +856,28 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                     if (k < C::NCH && n < N) prefetch_l2(args.aux + static_cast<size_t>(row) * args.ld_aux + n);
                 }
             }
+            // 512-wide GELU' epilogue: GELU'(H) of this warp's first chunk, computed while the
+            // tile's main loop still runs (the same function on the same H, so the same bits), so
+            // that accumulator half 0 is read out and released sooner. (Two chunks exceed the
+            // register budget of ten warps and spill.)
+            constexpr int PRE_N = (E == EPI_DGELU && C::NACC == 1) ? 1 : 0;
+            f32x2_t gpre[PRE_N > 0 ? PRE_N : 1][16];
+            if (PRE_N > 0 && part < 0) {
+#pragma unroll
+                for (int k = 0; k < PRE_N; ++k) {
+                    float hv[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = n0 + 32 * (eset + C::EPI_SETS * k) + 8 * i;
+                        const uint4 hw = (row < M && n < N)
+                                             ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
+                                             : make_uint4(0, 0, 0, 0);
+                        unpack_bf16x8(hw, hv + 8 * i);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) gpre[k][j] = gelu_grad_fast_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
+                }
+            }
             // One lane waits; the warp follows its verdict so the .sync.aligned TMEM loads
             // below always run with all 32 lanes.
             int ready = 0;
@@ -877,9 +899,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
             // gnext: Hg.
             uint4 hnext[4], gnext[4];
             if (E == EPI_DGELU || E == EPI_BIAS_DROPOUT_RES || E == EPI_DSWIGLU) {
+                const int c_first = eset + C::EPI_SETS * (part < 0 ? PRE_N : 0);  // past the precomputed chunks
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int n = n0 + 32 * eset + 8 * i;
+                    const int n = n0 + 32 * c_first + 8 * i;
                     const bool in = row < M && n < N;
                     hnext[i] = in ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n) : make_uint4(0, 0, 0, 0);
                     if (E == EPI_DSWIGLU)
@@ -1043,24 +1066,35 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                 }
                 float cs0 = 0.0f;  // GELU' epilogues: column sum of this warp's 32 rows, column nc + lane
                 if (E == EPI_DGELU) {
-                    float hv[32];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
-                    if (c + C::EPI_SETS < C::OBN / 32) {  // the next chunk of H into registers
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int n = nc + 32 * C::EPI_SETS + 8 * i;
-                            hnext[i] = (row < M && n < N)
-                                           ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
-                                           : make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    if (c + 3 * C::EPI_SETS < C::OBN / 32 && row < M && nc + 96 * C::EPI_SETS < N)  // and three ahead into L2
+                    if (c + 3 * C::EPI_SETS < C::OBN / 32 && row < M && nc + 96 * C::EPI_SETS < N)  // three ahead into L2
                         prefetch_l2(args.aux + static_cast<size_t>(row) * args.ld_aux + nc + 96 * C::EPI_SETS);
+                    // dH = dG GELU'(H), two columns at a time (constant indices into gpre only)
+                    auto apply = [&](const f32x2_t (&g)[16]) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {  // dH = dG GELU'(H), two columns at a time
-                        const f32x2_t gd = gelu_grad_fast_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
-                        f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), gd), v[2 * j], v[2 * j + 1]);
+                        for (int j = 0; j < 16; ++j)
+                            f2_unpack(f2_mul(f2_pack(v[2 * j], v[2 * j + 1]), g[j]), v[2 * j], v[2 * j + 1]);
+                    };
+                    if (PRE_N > 0 && wc == 0) {
+                        apply(gpre[0]);
+                    } else if (PRE_N > 1 && wc == 1) {
+                        apply(gpre[PRE_N > 1 ? 1 : 0]);
+                    } else {
+                        float hv[32];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) unpack_bf16x8(hnext[i], hv + 8 * i);
+                        if (c + C::EPI_SETS < C::OBN / 32) {  // the next chunk of H into registers
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int n = nc + 32 * C::EPI_SETS + 8 * i;
+                                hnext[i] = (row < M && n < N)
+                                               ? ldg_nc_v4(args.aux + static_cast<size_t>(row) * args.ld_aux + n)
+                                               : make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        f32x2_t g[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) g[j] = gelu_grad_fast_pair(f2_pack(hv[2 * j], hv[2 * j + 1]));
+                        apply(g);
                     }
                     if (args.colsum_rows) {  // this warp's 32 rows of dH, summed per column
                         float cs[32];
