@@ -353,11 +353,10 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
             }
             const int k0 = j * C::BKV;
             if ((args.causal && k0 + C::BKV - 1 > q0) || k0 + C::BKV > s) {  // CTA-uniform
+                // keys after min(s - 1, query) are masked: one compare per column
+                const int lim = min(s - 1, args.causal ? qi : 0x7fffffff) - k0;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int key = k0 + c;
-                    if (key >= s || (args.causal && key > qi)) x[c] = NEG_INF;
-                }
+                for (int c = 0; c < 64; ++c) x[c] = c > lim ? NEG_INF : x[c];
             }
             const float mx = max_tree(x) * c2;  // the scale is positive: max commutes with it
             const bool resc = mx > m_used + static_cast<float>(kLazyRescaleLog2);
@@ -648,22 +647,29 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1) attn_bwd_dkdv_kernel(cons
             }
             const int blk0 = (qb_first + i) * C::BQ;
             const bool need_mask = (args.causal && blk0 < k0 + C::BKV - 1) || blk0 + C::BQ > s || k0 + C::BKV > s;
+            float Dv[16];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 const float4 L4 = lds128f(sL + 16u * c4), D4 = lds128f(sD + 16u * c4);
-                const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+                const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+                Dv[4 * c4] = D4.x;
+                Dv[4 * c4 + 1] = D4.y;
+                Dv[4 * c4 + 2] = D4.z;
+                Dv[4 * c4 + 3] = D4.w;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 4 * c4 + e;
-                    float pv = ex2(fmaf(p[c], args.scale_log2, -Lv[e]));
-                    if (need_mask) {
-                        const int qi = qq0 + c;
-                        if (qi >= s || kj >= s || (args.causal && kj > qi)) pv = 0.0f;
-                    }
-                    p[c] = pv;
-                    dp[c] = pv * (dp[c] - Dv[e]);
-                }
+                for (int e = 0; e < 4; ++e) p[4 * c4 + e] = ex2(fmaf(p[4 * c4 + e], args.scale_log2, -Lv[e]));
             }
+            // Masked pairs (query past the sequence, key past it, or key after query) are zeroed
+            // by one compare per column against this thread's valid range of c: a test on
+            // need_mask per column would cost a branch each.
+            if (need_mask) {
+                const int c_lo = args.causal ? kj - qq0 : -(1 << 30);  // query >= key
+                const int c_hi = kj < s ? s - qq0 : -(1 << 30);        // query < s, key < s
+#pragma unroll
+                for (int c = 0; c < 16; ++c) p[c] = (c >= c_lo && c < c_hi) ? p[c] : 0.0f;
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) dp[c] = p[c] * (dp[c] - Dv[c]);
             {  // P^T and dS^T over the first 8 of the 16 S^T / dP^T columns this thread has read
                 uint32_t pk[8], dk[8];
 #pragma unroll
@@ -930,14 +936,14 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float pv = ex2(fmaf(p[c], args.scale_log2, nLq));
-                if (need_mask) {
-                    const int key = kk0 + cb + c;
-                    if (qi >= s || key >= s || (args.causal && key > qi)) pv = 0.0f;
-                }
-                dp[c] = pv * (dp[c] - Dq);
+            for (int c = 0; c < 32; ++c) p[c] = ex2(fmaf(p[c], args.scale_log2, nLq));
+            if (need_mask) {  // columns past lim are masked (key past the sequence or after the query)
+                const int lim = (qi >= s ? -1 : min(s - 1, args.causal ? qi : 0x7fffffff)) - (kk0 + cb);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) p[c] = c > lim ? 0.0f : p[c];
             }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) dp[c] = p[c] * (dp[c] - Dq);
             // dS_j goes where dS_{j-2} was: dQ_{j-2} must have read it
             if (j >= 2 && !warp_wait(b_dqd + 8 * pst, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
                                      DEV_TIMEOUT_EPILOGUE, 2006, j)) {
