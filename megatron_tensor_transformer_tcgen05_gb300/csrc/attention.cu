@@ -70,6 +70,51 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Pairs of fp32 values in one 64-bit register, for the sm_100-family f32x2 instructions: two
+// IEEE round-to-nearest operations each, so the same bits as the scalar forms at half the issue.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2(float lo, float hi)
+{
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma_(f2_t a, f2_t b, f2_t c)
+{
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_add_(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul_(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// x[c] = 2^(x[c] a + b) for N values, the fma on pairs
+template <int N>
+__device__ __forceinline__ void exp2_affine(float (&x)[N], float a, float b)
+{
+    const f2_t av = f2(a, a), bv = f2(b, b);
+#pragma unroll
+    for (int c = 0; c < N; c += 2) {
+        float lo, hi;
+        f2_split(f2_fma_(f2(x[c], x[c + 1]), av, bv), lo, hi);
+        x[c] = ex2(lo);
+        x[c + 1] = ex2(hi);
+    }
+}
+
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -146,12 +191,18 @@ __device__ __forceinline__ float max_tree(const float (&x)[N])
 template <int N>
 __device__ __forceinline__ float sum_tree(const float (&x)[N])
 {
-    float m[8];
+    // m[i] = x[i] + x[i + 8] + x[i + 16] + ... in that order, four pairs at a time
+    f2_t m[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = x[i];
+    for (int i = 0; i < 4; ++i) m[i] = f2(x[2 * i], x[2 * i + 1]);
 #pragma unroll
-    for (int c = 8; c < N; ++c) m[c & 7] += x[c];
-    return ((m[0] + m[1]) + (m[2] + m[3])) + ((m[4] + m[5]) + (m[6] + m[7]));
+    for (int c = 8; c < N; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m[i] = f2_add_(m[i], f2(x[c + 2 * i], x[c + 2 * i + 1]));
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2_split(m[i], v[2 * i], v[2 * i + 1]);
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 }
 
 struct FwdCfg {
@@ -370,8 +421,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_kernel(const __grid_constant_
                 l *= alpha;
             }
             const float nref = (m_used == NEG_INF) ? 0.0f : -m_used;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = ex2(fmaf(x[c], c2, nref));
+            exp2_affine(x, c2, nref);
             l += sum_tree(x);
             // O may be rescaled once PV_{j-1} has completed (only when some row's max grew)
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {
@@ -660,7 +710,14 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1) attn_bwd_dkdv_kernel(cons
                 Dv[4 * c4 + 2] = D4.z;
                 Dv[4 * c4 + 3] = D4.w;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) p[4 * c4 + e] = ex2(fmaf(p[4 * c4 + e], args.scale_log2, -Lv[e]));
+                for (int e = 0; e < 4; e += 2) {
+                    float lo, hi;
+                    f2_split(f2_fma_(f2(p[4 * c4 + e], p[4 * c4 + e + 1]), f2(args.scale_log2, args.scale_log2),
+                                     f2(-Lv[e], -Lv[e + 1])),
+                             lo, hi);
+                    p[4 * c4 + e] = ex2(lo);
+                    p[4 * c4 + e + 1] = ex2(hi);
+                }
             }
             // Masked pairs (query past the sequence, key past it, or key after query) are zeroed
             // by one compare per column against this thread's valid range of c: a test on
@@ -672,7 +729,9 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1) attn_bwd_dkdv_kernel(cons
                 for (int c = 0; c < 16; ++c) p[c] = (c >= c_lo && c < c_hi) ? p[c] : 0.0f;
             }
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dp[c] = p[c] * (dp[c] - Dv[c]);
+            for (int c = 0; c < 16; c += 2)  // dS^T = P^T (dP^T - D), on pairs
+                f2_split(f2_mul_(f2(p[c], p[c + 1]), f2_add_(f2(dp[c], dp[c + 1]), f2(-Dv[c], -Dv[c + 1]))), dp[c],
+                         dp[c + 1]);
             {  // P^T and dS^T over the first 8 of the 16 S^T / dP^T columns this thread has read
                 uint32_t pk[8], dk[8];
 #pragma unroll
@@ -938,15 +997,18 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1) attn_bwd_dq_kernel(const __
             if (lane == 0) mbar_arrive(b_spr);
             const int kk0 = j * C::BKV;
             const bool need_mask = (args.causal && kk0 + C::BKV - 1 > q0) || kk0 + C::BKV > s || q0 + C::BQ > s;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) p[c] = ex2(fmaf(p[c], args.scale_log2, nLq));
+            exp2_affine(p, args.scale_log2, nLq);
             if (need_mask) {  // columns past lim are masked (key past the sequence or after the query)
                 const int lim = (qi >= s ? -1 : min(s - 1, args.causal ? qi : 0x7fffffff)) - (kk0 + cb);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) p[c] = c > lim ? 0.0f : p[c];
             }
+            {  // dS = P (dP - D), on pairs
+                const f2_t nd = f2(-Dq, -Dq);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) dp[c] = p[c] * (dp[c] - Dq);
+                for (int c = 0; c < 32; c += 2)
+                    f2_split(f2_mul_(f2(p[c], p[c + 1]), f2_add_(f2(dp[c], dp[c + 1]), nd)), dp[c], dp[c + 1]);
+            }
             // dS_j goes where dS_{j-2} was: dQ_{j-2} must have read it
             if (j >= 2 && !warp_wait(b_dqd + 8 * pst, ((j - 2) >> 1) & 1, abort_flag, args.status, limit,
                                      DEV_TIMEOUT_EPILOGUE, 2006, j)) {
