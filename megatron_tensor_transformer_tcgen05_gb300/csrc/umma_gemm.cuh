@@ -175,15 +175,22 @@ __device__ __forceinline__ float ex2_approx(float z)
     return r;
 }
 
+__device__ __forceinline__ float rcp_approx_f(float d)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
 // GELU, tanh form, on a pair of values. With u = sqrt(2/pi) (x + 0.044715 x^3):
 //   1 + tanh u = 2 s,  s = sigmoid(2u) = 1 / (1 + e),  e = exp(-2u),
 //   GELU(x) = x s,     GELU'(x) = s + 2 x s (1 - s) u'(x),  u'(x) = sqrt(2/pi) (1 + 3 0.044715 x^2).
-// e = 2^z with z = -2 log2(e) u = x (c0 + c1 x^2): one special-function op per value. The
-// reciprocal 1 / (1 + e) runs on the FMA pipe: Newton's iteration r <- r + r (1 - d r) from
-// the integer estimate bits(r0) = R - bits(d), R = 0x7EF311C0 (chosen by search over all
-// mantissas: |r0 d - 1| <= 5.06% for every normal d); three steps leave <= 1 ulp. Since
+// e = 2^z with z = -2 log2(e) u = x (c0 + c1 x^2), and s = 1 / (1 + e) from the hardware's
+// approximate reciprocal (<= 1 ulp): two special-function ops per value. The epilogues and
+// the operand transform that evaluate it are bound by their instruction counts, not by that
+// pipe (a reciprocal by three Newton steps on the FMA pipe measured slower in both). Since
 // 1 - s = e s, s (1 - s) = s^2 e has no cancellation.
-// x is first raised to at least -kGeluFloor (z <= 117.9 there, so e, d and r0 stay normal
+// x is first raised to at least -kGeluFloor (z <= 117.9 there, so e and 1 + e stay normal
 // numbers): below it GELU(x) and GELU'(x) are below 3.1e-35 in magnitude, which is what the
 // clamped x gives, and a huge negative x can no longer meet a tiny s in x s. GELU' also caps
 // x at +kGeluFloor (GELU' = 1 in fp32 from there on), so that x^2 stays finite where e = 0.
@@ -192,29 +199,28 @@ struct GeluPair {
     f32x2_t x, x2, e, s;
 };
 
-__device__ __forceinline__ GeluPair gelu_sigmoid_pair(f32x2_t x)
+// x0, x1 already clamped as the caller needs
+__device__ __forceinline__ GeluPair gelu_sigmoid_clamped(float x0, float x1)
 {
     constexpr float kC0 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654);
     constexpr float kC1 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
     GeluPair g;
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    g.x = f2_pack(fmaxf(x0, -kGeluFloor), fmaxf(x1, -kGeluFloor));
+    g.x = f2_pack(x0, x1);
     g.x2 = f2_mul(g.x, g.x);
     float z0, z1;
     f2_unpack(f2_mul(g.x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
-    g.e = f2_pack(ex2_approx(z0), ex2_approx(z1));
-    const f32x2_t nd = f2_fma(g.e, f2_splat(-1.0f), f2_splat(-1.0f));  // -(1 + e)
-    float d0, d1;
-    f2_unpack(nd, d0, d1);
-    // bits(-(1 + e)) = bits(1 + e) + 2^31, so R - bits(1 + e) = (R + 2^31) - bits(-(1 + e))
-    f32x2_t r = f2_pack(__uint_as_float(0xFEF311C0u - __float_as_uint(d0)),
-                        __uint_as_float(0xFEF311C0u - __float_as_uint(d1)));
-    const f32x2_t one = f2_splat(1.0f);
-#pragma unroll
-    for (int i = 0; i < 3; ++i) r = f2_fma(r, f2_fma(nd, r, one), r);
-    g.s = r;
+    const float e0 = ex2_approx(z0), e1 = ex2_approx(z1);
+    g.e = f2_pack(e0, e1);
+    g.s = f2_pack(rcp_approx_f(1.0f + e0), rcp_approx_f(1.0f + e1));
     return g;
+}
+
+// for GELU: x raised to at least -kGeluFloor
+__device__ __forceinline__ GeluPair gelu_sigmoid_pair(f32x2_t x)
+{
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    return gelu_sigmoid_clamped(fmaxf(x0, -kGeluFloor), fmaxf(x1, -kGeluFloor));
 }
 
 __device__ __forceinline__ f32x2_t gelu_value_pair(const GeluPair& g) { return f2_mul(g.x, g.s); }
@@ -228,34 +234,13 @@ __device__ __forceinline__ f32x2_t gelu_grad_pair(const GeluPair& g)
     return f2_fma(q, w, g.s);
 }
 
-__device__ __forceinline__ float rcp_approx_f(float d)
-{
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
-    return r;
-}
-
-// GELU'(x) for the dH epilogue, which is bound by its instruction count, not by the
-// special-function pipe: the same e and formula, with s = 1 / (1 + e) from the hardware's
-// approximate reciprocal (one special-function op, <= 1 ulp) in place of the seed and three
-// Newton steps (eight FMA-pipe instructions a pair). G itself keeps the Newton form, whose
-// bits the GELU recompute's operand transform must reproduce without loading the
-// special-function pipe twice per value.
+// GELU'(x) on a pair: x clamped to [-kGeluFloor, kGeluFloor]
 __device__ __forceinline__ f32x2_t gelu_grad_fast_pair(f32x2_t x)
 {
-    constexpr float kC0 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654);
-    constexpr float kC1 = static_cast<float>(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
-    GeluPair g;
     float x0, x1;
     f2_unpack(x, x0, x1);
-    g.x = f2_pack(fminf(fmaxf(x0, -kGeluFloor), kGeluFloor), fminf(fmaxf(x1, -kGeluFloor), kGeluFloor));
-    g.x2 = f2_mul(g.x, g.x);
-    float z0, z1;
-    f2_unpack(f2_mul(g.x, f2_fma(g.x2, f2_splat(kC1), f2_splat(kC0))), z0, z1);
-    const float e0 = ex2_approx(z0), e1 = ex2_approx(z1);
-    g.e = f2_pack(e0, e1);
-    g.s = f2_pack(rcp_approx_f(1.0f + e0), rcp_approx_f(1.0f + e1));
-    return gelu_grad_pair(g);
+    return gelu_grad_pair(gelu_sigmoid_clamped(fminf(fmaxf(x0, -kGeluFloor), kGeluFloor),
+                                               fminf(fmaxf(x1, -kGeluFloor), kGeluFloor)));
 }
 
 // Scalar forms (the split-tail fixup): the pair code on (x, x), so every path gets the same bits.
