@@ -8,10 +8,16 @@
 
 namespace mlp {
 
+// What an epilogue does per output element, for the tile-width rule: round the accumulator
+// (+ bias); math on it (GELU, GELU', dropout and residual); or read two saved activations and
+// write two outputs (the SwiGLU derivative).
+enum EpiWeight : int { kEpiRound = 0, kEpiMath = 1, kEpiTwoAux = 2 };
 // CTA pairs take 512-wide tiles (25% fewer operand bytes per FLOP than 256-wide; one
 // accumulator, so each tile's epilogue delays the next tile's MMAs by about half an
 // epilogue) when N allows and the K loop is long enough to hide that delay: K >= 2048 for
 // the epilogues that only round the accumulator (+ bias), K >= 4096 for those with math.
+// The two-input, two-output epilogue keeps 256-wide tiles with two accumulators at any K
+// (its read-out on one 512-column accumulator measured 10% slower at K = 12288).
 constexpr int kWideMinK = 2048, kWideMinKMath = 4096;
 // Each part of a split tile runs at least this many 64-deep k blocks.
 constexpr int kMinSplitKb = 16;
@@ -32,18 +38,19 @@ struct GemmPlan {
 
 // Whether a GEMM of these sizes would take 512-wide pair tiles, so that clusters of four
 // (whose residency the caller looks up) are worth considering.
-inline bool plan_wants_wide(int M, int N, int K, int bn, bool math)
+inline bool plan_wants_wide(int M, int N, int K, int bn, int weight)
 {
-    return bn >= 256 && M > 128 && N % 512 == 0 && K >= (math ? kWideMinKMath : kWideMinK);
+    return bn >= 256 && M > 128 && N % 512 == 0 && weight != kEpiTwoAux &&
+           K >= (weight == kEpiMath ? kWideMinKMath : kWideMinK);
 }
 
 // The plan for D[M,N] = sum_k A[m,k] B[n,k] on num_sms SMs.
 //   bn: 256 when the N extent the entry point tiles by is a multiple of 256, else 128.
-//   math: the epilogue computes more than a rounding (+ bias) of the accumulator.
+//   weight: the epilogue's EpiWeight.
 //   splittable: the split-tail fixup can finish this epilogue.
 //   quads: clusters of four CTAs that fit at once (0: unknown or none).
 //   split_ws_bytes: room for split parts (0: no split).
-inline GemmPlan plan_gemm(int M, int N, int K, int bn, bool math, bool splittable, int num_sms, int quads,
+inline GemmPlan plan_gemm(int M, int N, int K, int bn, int weight, bool splittable, int num_sms, int quads,
                           size_t split_ws_bytes)
 {
     GemmPlan p;
@@ -52,7 +59,7 @@ inline GemmPlan plan_gemm(int M, int N, int K, int bn, bool math, bool splittabl
     // otherwise sweep N fastest so they share one A block.
     p.n_fastest = M > N ? 1 : 0;
     const bool pairs = bn >= 256 && M > 128;
-    if (pairs && plan_wants_wide(M, N, K, bn, math)) bn = 512;
+    if (pairs && plan_wants_wide(M, N, K, bn, weight)) bn = 512;
     p.bn = bn;
     p.cg = pairs ? 2 : 1;
     p.tm = pairs ? 256 : 128;

@@ -8,8 +8,6 @@ template cudaError_t launch_umma_gemm<256, false, true, EPI_SWIGLU, 2>(const Gem
 template cudaError_t launch_umma_gemm<128, false, false, EPI_DSWIGLU, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DSWIGLU, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, false, EPI_DSWIGLU, 2>(const GemmArgs&, int, cudaStream_t);
-template cudaError_t launch_umma_gemm<512, false, false, EPI_DSWIGLU, 2>(const GemmArgs&, int, cudaStream_t);
-template int umma_gemm_max_clusters<512, false, false, EPI_DSWIGLU, 2>(int, int);
 template cudaError_t launch_umma_gemm<128, false, true, EPI_PLAIN, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, true, EPI_PLAIN, 1>(const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_umma_gemm<256, false, true, EPI_PLAIN, 2>(const GemmArgs&, int, cudaStream_t);

@@ -175,12 +175,18 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     constexpr int kEpiB = (EPI == EPI_PLAIN_GA) ? EPI_PLAIN : (EPI == EPI_BIAS_GA) ? EPI_BIAS : EPI;
     constexpr bool kSplittable =
         (kEpiB == EPI_PLAIN || kEpiB == EPI_BIAS || kEpiB == EPI_BIAS_GELU || kEpiB == EPI_DGELU);
-    const bool kMath = tiles_as_math >= 0 ? tiles_as_math != 0 : !(kEpiB == EPI_PLAIN || kEpiB == EPI_BIAS);
+    // the SwiGLU derivative never takes 512-wide tiles (gemm_plan.h), so none is built for it
+    constexpr bool kMayWide = kEpiB != EPI_DSWIGLU;
+    const int weight = tiles_as_math >= 0 ? (tiles_as_math != 0 ? kEpiMath : kEpiRound)
+                       : (kEpiB == EPI_PLAIN || kEpiB == EPI_BIAS) ? kEpiRound
+                       : kMayWide                                   ? kEpiMath
+                                                                    : kEpiTwoAux;
     if (!kSplittable || !so || !so->ws || !so->out) so = nullptr;
     int quads = 0;  // looked up only when two-pair clusters are possible
-    if (kClusterPairs && plan_wants_wide(g.M, g.N, g.K, BN, kMath) && ((g.M + 255) / 256) % 2 == 0)
-        quads = quad_clusters<A_MN, B_MN, EPI>(num_sms);
-    const GemmPlan p = plan_gemm(g.M, g.N, g.K, BN, kMath, kSplittable, num_sms, quads, so ? so->ws_bytes : 0);
+    if constexpr (kMayWide)
+        if (kClusterPairs && plan_wants_wide(g.M, g.N, g.K, BN, weight) && ((g.M + 255) / 256) % 2 == 0)
+            quads = quad_clusters<A_MN, B_MN, EPI>(num_sms);
+    const GemmPlan p = plan_gemm(g.M, g.N, g.K, BN, weight, kSplittable, num_sms, quads, so ? so->ws_bytes : 0);
     g.n_fastest = p.n_fastest;
     g.raster_group = p.raster_group;
     g.cluster_pairs = p.cluster_pairs;
@@ -189,10 +195,13 @@ static cudaError_t gemm(GemmArgs& g, int BN, int num_sms, cudaStream_t s, const 
     g.split_ws = p.split_tiles > 0 ? so->ws : nullptr;
     if (p.grid <= 0) return cudaSuccess;
     cudaError_t e;
-    if (p.cg == 2)
-        e = p.bn == 512 ? launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, p.grid, s)
-                        : launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, p.grid, s);
-    else
+    if (p.cg == 2) {
+        if constexpr (kMayWide)
+            e = p.bn == 512 ? launch_umma_gemm<512, A_MN, B_MN, EPI, 2>(g, p.grid, s)
+                            : launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, p.grid, s);
+        else
+            e = launch_umma_gemm<256, A_MN, B_MN, EPI, 2>(g, p.grid, s);
+    } else
         e = p.bn == 256 ? launch_umma_gemm<256, A_MN, B_MN, EPI, 1>(g, p.grid, s)
                         : launch_umma_gemm<128, A_MN, B_MN, EPI, 1>(g, p.grid, s);
     if (e != cudaSuccess) return e;

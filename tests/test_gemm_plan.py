@@ -61,6 +61,12 @@ def test_width_and_cluster_rules(plan):
     assert plan(4096, 12288, 2048)["bn"] == 512
     assert plan(4096, 12288, 2304, math=True)["bn"] == 256
     assert plan(4096, 12288, 4096, math=True)["bn"] == 512
+    # the SwiGLU derivative (two saved activations in, two outputs) never, at any K: the 175B
+    # SwiGLU dU GEMM runs 16 x 128 tiles of 256 x 256 on CTA pairs
+    p = plan(4096, 32768, 12288, math=2, splittable=False)
+    assert (p["bn"], p["cg"], p["cluster_pairs"], p["tm"], p["tiles"]) == (256, 2, 1, 256, 16 * 128)
+    assert all(plan(M, N, K, math=2)["bn"] == 256 for M, N, K in itertools.product((512, 4096), (512, 32768),
+                                                                                    (2048, 65536)))
     # N not a multiple of 512, or at most 128 rows: no 512-wide tiles
     assert plan(4096, 2304, 9216)["bn"] == 256
     assert (plan(128, 12288, 49152)["cg"], plan(128, 12288, 49152)["bn"]) == (1, 256)
@@ -88,7 +94,7 @@ SHAPES = list(itertools.product([1, 128, 300, 512, 2048, 4096, 16384], [8, 200, 
 
 @pytest.mark.parametrize("sms,quads", [(152, 36), (148, 37), (132, 0)])
 def test_plans_cover_every_tile_and_k_block_once(plan, sms, quads):
-    for (M, N, K), math, bn in itertools.product(SHAPES, (False, True), (128, 256)):
+    for (M, N, K), math, bn in itertools.product(SHAPES, (0, 1, 2), (128, 256)):
         if bn == 256 and N % 256:
             continue
         p = plan(M, N, K, bn=bn, math=math, sms=sms, quads=quads)
