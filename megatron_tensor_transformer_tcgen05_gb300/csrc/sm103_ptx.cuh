@@ -235,6 +235,14 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensor
         : "memory");
 }
 
+// global -> L2 only, the 2-D tile a tma_load_2d with the same map and coordinates would copy.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // shared -> global, 2-D tile; rows/columns beyond the tensor's extent are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int x, int y, uint32_t src)
 {

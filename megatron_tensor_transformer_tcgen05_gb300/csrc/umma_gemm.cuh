@@ -593,6 +593,29 @@ __global__ void __launch_bounds__(GemmCfg<BN, A_MN, B_MN, EPI, CG>::THREADS, 1) 
                                                  n0 + C::MMA_N * h + 128 * static_cast<int>(rank), fb0);
                         }
                     }
+                    // Transform flavours: a fill waits for its load, its transform and its MMAs in
+                    // series, and with four stages that round trip nearly sets the rate. The A and B
+                    // blocks one ring ahead are pulled into L2 now, so their loads do not wait on DRAM.
+                    if (C::XFORM && kb + C::STAGES < kb_hi) {
+                        const int k1 = (kb + C::STAGES) * C::BK;
+                        if (A_MN) {
+                            tma_prefetch_l2_2d(tA, m_cta, k1);
+                            tma_prefetch_l2_2d(tA, m_cta + 64, k1);
+                        } else {
+                            tma_prefetch_l2_2d(tA, k1, m_cta);
+                        }
+#pragma unroll
+                        for (int h = 0; h < C::HALVES; ++h) {
+                            if (npc == 2 && h != static_cast<int>(pidx)) continue;  // the other pair's half
+                            const int nb = n0 + C::MMA_N * h + 128 * static_cast<int>(rank);
+                            if (B_MN) {
+                                tma_prefetch_l2_2d(tB, nb, k1);
+                                tma_prefetch_l2_2d(tB, nb + 64, k1);
+                            } else {
+                                tma_prefetch_l2_2d(tB, k1, nb);
+                            }
+                        }
+                    }
                     issued |= 1u << stage;
                     par = (par & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
