@@ -1,7 +1,6 @@
 """Host-side checks of the C ABI: the library builds for sm_103a, loads without a GPU,
 exports every function the header declares, and rejects bad arguments before it touches
 the GPU (these calls fail in argument checking, so they never reach CUDA)."""
-import ctypes
 
 import pytest
 
